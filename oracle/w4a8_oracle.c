@@ -1,0 +1,212 @@
+/*
+ * w4a8_oracle.c -- plain, slow CPU reference of the W4A8 block-32 linear.
+ *
+ * TEST INFRASTRUCTURE ONLY: used by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg, never by the product path.  It shares no
+ * code with the CUDA library.  Build flags: -O2 -ffp-contract=off, no fast
+ * math, so every fp32 operation below is one IEEE binary32 operation with
+ * round-to-nearest-even, in the order written.
+ *
+ * Sources (pages on ML Drift, Google's on-device GPU inference engine):
+ *   [P1] "Що змінює ML Drift для on-device AI-інференсу на вашому телефоні?"
+ *        (tech.dede.sh), section "Stage-aware оптимізація для великих мовних
+ *        моделей": LLM benchmarks use 4-bit weights with block size 32;
+ *        decoding quantises activations inside the kernel to avoid moving
+ *        data through memory.
+ *   [P2] "谷歌突然开源！端侧 AI 的 GPU 底座，要变了" (m.x-techcon.com),
+ *        section "对大模型，重点已经从“算得快”变成“数据少搬”": in-kernel
+ *        activation quantisation during decode.
+ * The pages give no formula for the quantiser or the accumulation.  The
+ * reading implemented here (symmetric int8 per token and per 32-block,
+ * scale amax/127 in fp32, amax 0 -> scale 1, round half to even, clamp to
+ * +-127; int32 dot per block times s_w*s_x, summed in fp32 in ascending
+ * block order; fp16 output rounded to nearest even) is the plainest one the
+ * pages support.
+ *
+ * Pinned by tests/test_oracle_pins.py (closed forms, hand vectors, brute
+ * force, fp64 bound, invariants).
+ */
+#include "w4a8_oracle.h"
+
+#include <fenv.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define BLOCK 32
+
+/* ---- IEEE binary16 (sign 1, exponent 5 with bias 15, fraction 10) ---- */
+
+float oracle_half_to_float(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    float v;
+    if (e == 0) {
+        v = ldexpf((float)m, -24);                 /* zero or subnormal: m * 2^-24 */
+    } else if (e == 31) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexpf((float)(m | 0x400), e - 25);    /* (1024+m) * 2^(e-15-10) */
+    }
+    return sign ? -v : v;
+}
+
+uint16_t oracle_float_to_half(float f)
+{
+    uint16_t sign = signbit(f) ? 0x8000u : 0u;
+    if (isnan(f)) return (uint16_t)(sign | 0x7e00u);
+    float a = fabsf(f);
+    /* 65520 is halfway between 65504 (largest finite, odd fraction) and
+     * 2^16; the tie goes to the even neighbour, which is infinity. */
+    if (a >= 65520.0f) return (uint16_t)(sign | 0x7c00u);
+    if (a < 0x1p-14f) {
+        /* subnormal range: a = m * 2^-24 with m rounded half to even.
+         * m == 1024 is the smallest normal, whose encoding is also 1024. */
+        float m = nearbyintf(a * 0x1p24f);
+        return (uint16_t)(sign | (uint16_t)m);
+    }
+    int ex;
+    (void)frexpf(a, &ex);            /* a = fr * 2^ex, fr in [0.5, 1) */
+    int E = ex - 1;                  /* a in [2^E, 2^(E+1)) */
+    float t = nearbyintf(ldexpf(a, 10 - E));   /* in [1024, 2048] */
+    if (t == 2048.0f) { t = 1024.0f; E += 1; }
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)((int)t - 1024));
+}
+
+/* ---- activation quantisation (steps a1-a3) ---- */
+
+/* One token, one 32-wide block: amax, scale, codes.  Returns -2 if the block
+ * holds a non-finite value (outside the operator's domain). */
+static int quantize_block(const uint16_t *xb, int8_t *qb, float *s_out)
+{
+    float xf[BLOCK];
+    float amax = 0.0f;
+    for (int k = 0; k < BLOCK; ++k) {
+        xf[k] = oracle_half_to_float(xb[k]);
+        if (!isfinite(xf[k])) return -2;
+        float a = fabsf(xf[k]);
+        if (a > amax) amax = a;
+    }
+    float s = (amax == 0.0f) ? 1.0f : amax / 127.0f;
+    for (int k = 0; k < BLOCK; ++k) {
+        float v = xf[k] / s;              /* one fp32 division, rounded to nearest even */
+        float r = nearbyintf(v);          /* ties to even in the default rounding mode */
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        qb[k] = (int8_t)(int)r;
+    }
+    *s_out = s;
+    return 0;
+}
+
+int oracle_quantize_act(const uint16_t *x, int M, int K, int8_t *q, float *sx)
+{
+    if (M < 0 || K <= 0 || K % BLOCK != 0) return -1;
+    if (fegetround() != FE_TONEAREST) return -3;
+    int nb = K / BLOCK;
+    for (int m = 0; m < M; ++m)
+        for (int b = 0; b < nb; ++b) {
+            int rc = quantize_block(x + (size_t)m * K + (size_t)b * BLOCK,
+                                    q + (size_t)m * K + (size_t)b * BLOCK,
+                                    sx + (size_t)m * nb + b);
+            if (rc) return rc;
+        }
+    return 0;
+}
+
+/* ---- per-block integer dot (step a5) ---- */
+
+int oracle_block_dots(const int8_t *q, const int8_t *w, int M, int N, int K,
+                      int32_t *d)
+{
+    if (M < 0 || N < 0 || K <= 0 || K % BLOCK != 0) return -1;
+    int nb = K / BLOCK;
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n)
+            for (int b = 0; b < nb; ++b) {
+                int32_t acc = 0;
+                for (int k = b * BLOCK; k < (b + 1) * BLOCK; ++k)
+                    acc += (int32_t)w[(size_t)n * K + k] * (int32_t)q[(size_t)m * K + k];
+                d[((size_t)m * N + n) * nb + b] = acc;
+            }
+    return 0;
+}
+
+/* ---- the whole linear (steps a1-a8) ---- */
+
+int oracle_linear(const uint16_t *x, const int8_t *w, const uint16_t *sw,
+                  int M, int N, int K, uint16_t *y, float *acc_out)
+{
+    if (M < 0 || N < 0 || K <= 0 || K % BLOCK != 0) return -1;
+    int nb = K / BLOCK;
+    int8_t *q = (int8_t *)malloc((size_t)K);
+    float *sx = (float *)malloc(sizeof(float) * (size_t)nb);
+    if (!q || !sx) { free(q); free(sx); return -4; }
+    int rc = 0;
+    for (int m = 0; m < M && rc == 0; ++m) {
+        rc = oracle_quantize_act(x + (size_t)m * K, 1, K, q, sx);
+        if (rc) break;
+        for (int n = 0; n < N; ++n) {
+            const int8_t *wr = w + (size_t)n * K;
+            float acc = 0.0f;
+            for (int b = 0; b < nb; ++b) {
+                int32_t d = 0;
+                for (int k = b * BLOCK; k < (b + 1) * BLOCK; ++k)
+                    d += (int32_t)wr[k] * (int32_t)q[k];
+                float p = oracle_half_to_float(sw[(size_t)n * nb + b]) * sx[b];
+                float t = (float)d * p;   /* exact conversion: |d| <= 32*8*127 < 2^24 */
+                acc = acc + t;
+            }
+            if (acc_out) acc_out[(size_t)m * N + n] = acc;
+            y[(size_t)m * N + n] = oracle_float_to_half(acc);
+        }
+    }
+    free(q);
+    free(sx);
+    return rc;
+}
+
+int oracle_linear_f64(const uint16_t *x, const int8_t *w, const uint16_t *sw,
+                      int M, int N, int K, double *ref)
+{
+    if (M < 0 || N < 0 || K <= 0 || K % BLOCK != 0) return -1;
+    int nb = K / BLOCK;
+    int8_t *q = (int8_t *)malloc((size_t)K);
+    float *sx = (float *)malloc(sizeof(float) * (size_t)nb);
+    if (!q || !sx) { free(q); free(sx); return -4; }
+    int rc = 0;
+    for (int m = 0; m < M && rc == 0; ++m) {
+        rc = oracle_quantize_act(x + (size_t)m * K, 1, K, q, sx);
+        if (rc) break;
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int b = 0; b < nb; ++b) {
+                double swd = (double)oracle_half_to_float(sw[(size_t)n * nb + b]);
+                double sxd = (double)sx[b];
+                for (int k = b * BLOCK; k < (b + 1) * BLOCK; ++k)
+                    acc += (swd * (double)w[(size_t)n * K + k]) * (sxd * (double)q[k]);
+            }
+            ref[(size_t)m * N + n] = acc;
+        }
+    }
+    free(q);
+    free(sx);
+    return rc;
+}
+
+/* ---- packed-weight reader ---- */
+
+int oracle_unpack_weights(const uint8_t *packed, int N, int K, int8_t *w)
+{
+    if (N < 0 || K <= 0 || K % BLOCK != 0) return -1;
+    size_t row_bytes = (size_t)K / 2;
+    for (int n = 0; n < N; ++n)
+        for (size_t j = 0; j < row_bytes; ++j) {
+            uint8_t byte = packed[(size_t)n * row_bytes + j];
+            w[(size_t)n * K + 2 * j] = (int8_t)((int)(byte & 0x0f) - 8);
+            w[(size_t)n * K + 2 * j + 1] = (int8_t)((int)(byte >> 4) - 8);
+        }
+    return 0;
+}

@@ -1,0 +1,69 @@
+/*
+ * w4a8_oracle.h -- plain, slow CPU reference of the W4A8 block-32 linear.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library
+ * and its Python binding) may include, link or call this code; only the
+ * tests, the smoke check and the benchmark's CPU-baseline leg do.  It shares
+ * no source, header, table or helper with the CUDA path.
+ *
+ * What the method computes, and where it comes from:
+ *   - 4-bit weights grouped in blocks of 32 along K, fp16 block scales, and
+ *     activations quantised inside the kernel while decoding
+ *     ("Що змінює ML Drift для on-device AI-інференсу на вашому телефоні?",
+ *      tech.dede.sh, section "Stage-aware оптимізація для великих мовних
+ *      моделей"; "谷歌突然开源！端侧 AI 的 GPU 底座，要变了", m.x-techcon.com,
+ *      section "对大模型，重点已经从“算得快”变成“数据少搬”").
+ *   - The pages leave the quantiser's arithmetic open.  Reading taken here:
+ *     symmetric int8 per token and per 32-wide block of K, scale amax/127 in
+ *     fp32 (amax 0 gives scale 1), round half to even, clamp to [-127,127];
+ *     each block's integer dot is multiplied by s_w*s_x and summed in fp32;
+ *     the result is written as fp16 with round-to-nearest-even.
+ *
+ * All fp16 values cross this interface as their IEEE binary16 bit patterns
+ * (uint16_t).  All arrays are dense row-major.  Functions return 0 on
+ * success and a negative number on a bad argument.
+ */
+#ifndef W4A8_ORACLE_H
+#define W4A8_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* IEEE binary16 <-> binary32, written from the format definition. */
+float    oracle_half_to_float(uint16_t h);
+uint16_t oracle_float_to_half(float f);
+
+/* Activation quantisation: x [M][K] fp16 -> codes q [M][K] int8 and scales
+ * sx [M][K/32] fp32.  K must be a positive multiple of 32. */
+int oracle_quantize_act(const uint16_t *x, int M, int K, int8_t *q, float *sx);
+
+/* Per-block integer dots: d[m][n][b] = sum_{k in block b} w[n][k]*q[m][k].
+ * w [N][K] int8 weight codes, q [M][K] int8 activation codes. */
+int oracle_block_dots(const int8_t *q, const int8_t *w, int M, int N, int K,
+                      int32_t *d);
+
+/* The whole linear: y [M][N] fp16 = sum_b float(d_b) * (s_w * s_x) in fp32.
+ * w [N][K] int8 codes in [-8,7]; sw [N][K/32] fp16.  acc (may be NULL)
+ * receives the fp32 sums before the fp16 rounding. */
+int oracle_linear(const uint16_t *x, const int8_t *w, const uint16_t *sw,
+                  int M, int N, int K, uint16_t *y, float *acc);
+
+/* Checker: the same dequantised product in fp64,
+ * ref[m][n] = sum_b sum_k (double)sw*w * (double)sx*q, with the codes and
+ * activation scales of oracle_quantize_act. */
+int oracle_linear_f64(const uint16_t *x, const int8_t *w, const uint16_t *sw,
+                      int M, int N, int K, double *ref);
+
+/* Reads the packed weight layout of the library's public header from its
+ * written definition: row n occupies K/2 bytes; byte j holds weight k=2j in
+ * its low nibble and k=2j+1 in its high nibble, each stored as w+8. */
+int oracle_unpack_weights(const uint8_t *packed, int N, int K, int8_t *w);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
