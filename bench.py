@@ -1,0 +1,362 @@
+"""Benchmark of the W4A8 block-32 linear on GB300.
+
+Headline workload: decode FFN up-projection, M=1, K=2048, N=8192, with 16
+distinct weight sets (151 MB of packed weights and scales, more than the
+129 MB L2) used in rotation, so every call streams its weights from HBM.
+A step is one CUDA-graph replay of `--calls-per-step` consecutive decode
+calls cycling through the 16 sets.  The metric is effective HBM bandwidth:
+algorithmic bytes (int4 weights + fp16 block scales + fp16 x + fp16 y) per
+second.  Secondary lines in the same JSON record the prefill GEMM
+(M=512, K=2048, N=8192) in int8-equivalent TOPS (2*M*N*K per call).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica (the linear has no
+exchange step on one GPU); rank 0 prints one JSON line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "decode_ffn_up_m1_k2048_n8192"
+METRIC = "W4A8 linear: decode eff. HBM GB/s & prefill int8 TOPS, % of GB300 roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--calls-per-step", type=int, default=512)
+    ap.add_argument("--sets", type=int, default=16)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            hbm = d.get("hbm_gbs")
+            bf16 = d.get("bf16_tflops")
+            if hbm and bf16:
+                return float(hbm), float(bf16), float(d.get("bf16_tflops_sustained") or bf16), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, files):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p)).get(kernel)
+    except Exception:
+        return None
+    if not d or d.get("source_hash") != kernel_hash(files):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_inputs(lin, seed):
+    from int4_weight_quantized_gb300 import workloads as wl
+    x, codes, scales = wl.make_linear_inputs(lin, seed, 0)
+    return x.numpy(), codes.numpy(), scales.numpy()
+
+
+def time_oracle(inputs, seconds, max_calls=None):
+    """The CPU oracle on this host, as it stands, on whole calls until `seconds` pass."""
+    import oracle
+    xn, cn, sn = inputs
+    oracle.get()
+    calls = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.linear(xn, cn, sn)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_calls and calls >= max_calls):
+            break
+    return calls, el
+
+
+def reference_arm(args):
+    """The oracle timed on host cores: same metric, unit and workload as our arm.
+    A step is one whole decode call (M=1, K=2048, N=8192) of the oracle."""
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    from int4_weight_quantized_gb300 import workloads as wl
+    W = [w for w in wl.workloads() if w.name == HEADLINE][0]
+    lin = W.linears[0]
+    inputs = oracle_inputs(lin, W.seed)
+    time_oracle(inputs, 0.0, max_calls=max(1, args.warmup))
+    calls, secs = time_oracle(inputs, 1e9, max_calls=args.steps)
+    gbs = lin.bytes * calls / secs / 1e9
+    sample = f"{calls} whole M=1 K=2048 N=8192 calls of the plain C oracle, single thread"
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": calls, "warmup": args.warmup, "ms_per_step": 1e3 * secs / calls,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4xint8",
+            "data": "synthetic", "config": {"workload": HEADLINE, "calls_per_step": 1},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import int4_weight_quantized_gb300 as w4
+    from int4_weight_quantized_gb300 import workloads as wl
+    from int4_weight_quantized_gb300.build import build
+    if rank == 0:
+        build()
+    if ws > 1:
+        dist.barrier()
+    build()
+
+    W = [w for w in wl.workloads() if w.name == HEADLINE][0]
+    lin = W.linears[0]
+    S = args.sets
+    dev = torch.device("cuda", local)
+    xs = wl.make_x(lin.M, lin.K, W.seed, lin.outlier_frac).to(dev)
+    sets = []
+    for i in range(S):
+        codes, scales = wl.make_weights(lin.N, lin.K, W.seed + 1 + i, lin.s_lo, lin.s_hi)
+        sets.append((w4.pack(codes.to(dev)), scales.to(dev)))
+    outs = [torch.empty((lin.M, lin.N), dtype=torch.float16, device=dev) for _ in range(S)]
+    cps = args.calls_per_step
+
+    def step_calls():
+        for c in range(cps):
+            i = c % S
+            w4.linear(xs, sets[i][0], sets[i][1], out=outs[i], path=w4.PATH_DECODE)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        step_calls()                                  # first call sets kernel attributes
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step_calls()
+        for _ in range(args.warmup):
+            g.replay()
+        stream.synchronize()
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk:
+            e0.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    bytes_step = lin.bytes * cps
+    value = ws * bytes_step * args.steps / (ms * 1e-3) / 1e9
+    per_launch_s = ms * 1e-3 / (args.steps * cps)
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    gemv_files = ["int4_weight_quantized_gb300/csrc/gemv.cu", "int4_weight_quantized_gb300/csrc/common.cuh"]
+    achieved = lin.bytes / per_launch_s / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": traffic_for("gemv_decode_ffn_up", gemv_files), "peak_source": peak_src,
+            "kernel": "gemv_kernel<1,4,false>", "algorithmic_bytes_per_launch": lin.bytes}
+
+    # ---- end to end through the C entry point with pinned host buffers
+    e2e_steps = max(3, min(args.steps, 50))
+    xh = torch.empty((cps, lin.M, lin.K), dtype=torch.float16).pin_memory()
+    xh.copy_(xs.cpu().expand(cps, lin.M, lin.K))
+    yh = torch.empty((cps, lin.M, lin.N), dtype=torch.float16).pin_memory()
+    xd = torch.empty((cps, lin.M, lin.K), dtype=torch.float16, device=dev)
+    yd = torch.empty((cps, lin.M, lin.N), dtype=torch.float16, device=dev)
+    with torch.cuda.stream(stream):
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            for c in range(cps):
+                i = c % S
+                w4.linear_c(xd[c], sets[i][0], sets[i][1], yd[c])
+            yh.copy_(yd, non_blocking=True)
+            stream.synchronize()
+        e2e_step()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e2e_s = time.perf_counter() - t0
+    e2e_val = ws * bytes_step * e2e_steps / e2e_s / 1e9
+    e2e = {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": xh.numel() * 2,
+           "d2h_bytes_per_step": yh.numel() * 2, "steps": e2e_steps,
+           "note": "w4a8_linear per call, eager launches, inputs copied from pinned host each step, outputs read back"}
+
+    secondary = []
+    if not args.no_secondary:
+        secondary = run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src)
+
+    cpu = None
+    if rank == 0:
+        calls, secs = time_oracle(oracle_inputs(lin, W.seed), args.cpu_seconds)
+        cpu = {"value": lin.bytes * calls / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{calls} whole M=1 K=2048 N=8192 calls of the plain C oracle in {secs:.1f} s, single thread"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "int4xint8", "data": "synthetic",
+                "config": {"workload": HEADLINE, "M": lin.M, "N": lin.N, "K": lin.K, "weight_sets": S,
+                           "calls_per_step": cps, "l2": f"inputs larger than L2: {S} rotating weight sets = "
+                           f"{S * lin.weight_bytes / 1e6:.1f} MB > 129 MB",
+                           "launch": "CUDA graph of calls_per_step decode launches", "parallelism": f"replicas{ws}"},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps * cps, "clocks": clk.summary(), "secondary": secondary}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src):
+    """Prefill GEMM (M=512) in TOPS, timed with CUDA events on its stream."""
+    import torch
+    res = []
+    W = [w for w in wl.workloads() if w.name == "prefill_ffn_up_m512_k2048_n8192"][0]
+    lin = W.linears[0]
+    x, codes, scales = wl.make_linear_inputs(lin, W.seed, 0)
+    xd = x.to(dev)
+    sets = []
+    for i in range(4):
+        c, s = wl.make_weights(lin.N, lin.K, W.seed + 1 + i, lin.s_lo, lin.s_hi)
+        sets.append((w4.pack(c.to(dev)), s.to(dev)))
+    out = torch.empty((lin.M, lin.N), dtype=torch.float16, device=dev)
+    ws = w4.make_workspace(lin.M, lin.N, lin.K, w4.PATH_PREFILL, dev)
+    reps = 8
+    with torch.cuda.stream(stream):
+        def calls():
+            for r in range(reps):
+                p, s = sets[r % len(sets)]
+                w4.linear(xd, p, s, out=out, path=w4.PATH_PREFILL, workspace=ws)
+        calls()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            calls()
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = 20
+        e0.record(stream)
+        for _ in range(n):
+            g.replay()
+        e1.record(stream)
+        e1.synchronize()
+    per_call = e0.elapsed_time(e1) * 1e-3 / (n * reps)
+    tops = lin.ops / per_call / 1e12
+    res.append({"workload": W.name, "value": tops, "unit": "TOPS (2*M*N*K int8-equivalent)",
+                "us_per_call": per_call * 1e6,
+                "roofline": {"bound": "tensor", "achieved": tops, "peak": bf16, "unit": "TFLOP/s",
+                             "frac": tops / bf16, "peak_source": peak_src,
+                             "note": "contraction runs on fp16 tensor cores (exact for int4 x int8 codes); "
+                                     "peak is the dense fp16/bf16 tensor rate"}})
+    return res
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * w4a8.h -- C ABI of the GB300 (sm_103a) W4A8 block-32 linear.
+ *
+ * The operator: y = x * W^T for a linear layer whose weights are 4-bit
+ * integers in blocks of 32 along K with one fp16 scale per block, and whose
+ * fp16 activations are quantised to int8 inside the kernel, per token and per
+ * 32-wide block.  The pages that describe it (Google's ML Drift engine):
+ *   "Що змінює ML Drift для on-device AI-інференсу на вашому телефоні?"
+ *   (tech.dede.sh), section "Stage-aware оптимізація для великих мовних
+ *   моделей": 4-bit weights with block size 32; prefill is compute-bound and
+ *   decode memory-bound; kernels and layouts switch with the phase; decode
+ *   quantises activations inside the kernel to avoid extra memory traffic.
+ *   "谷歌突然开源！端侧 AI 的 GPU 底座，要变了" (m.x-techcon.com), section
+ *   "对大模型，重点已经从“算得快”变成“数据少搬”": the same stage-aware
+ *   kernel choice and in-kernel activation quantisation.
+ * The pages leave the arithmetic open; this library implements the plainest
+ * reading they support:
+ *   s_x[m,b] = amax_{k in b} |x[m,k]| / 127 in fp32 (amax 0 gives 1),
+ *   q[m,k]   = clamp(round_half_even(x[m,k] / s_x[m,b]), -127, 127),
+ *   d[m,n,b] = sum_{k in b} w[n,k] * q[m,k]            (exact integer),
+ *   y[m,n]   = fp16_rne( sum_b d[m,n,b] * (s_w[n,b] * s_x[m,b]) )  in fp32.
+ * Codes and block dots are exact; the fp32 sum's order and fusion are the
+ * kernel's, so y matches a sequential fp32 sum to within rounding.
+ *
+ * Conventions for every entry point:
+ *   - fp16 tensors are passed as IEEE binary16 bit patterns (uint16_t).
+ *   - Every tensor is dense row-major device memory, allocated and owned by
+ *     the caller; pointers must be 16-byte aligned.
+ *   - Calls are asynchronous and ordered on `stream` unless stated otherwise;
+ *     nothing is allocated per call except by w4a8_linear on the prefill path
+ *     (stream-ordered, see there).  Distinct streams may be used from
+ *     distinct host threads.
+ *   - Errors are returned, never raised: no entry point aborts, exits or
+ *     traps the GPU.  Argument errors are detected before anything is
+ *     launched.  W4A8_ERR_CUDA means a CUDA call or launch failed; the
+ *     pending CUDA error is consumed (cudaGetLastError) when it is reported.
+ */
+#ifndef W4A8_H
+#define W4A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4A8_OK = 0,
+    W4A8_ERR_INVALID_VALUE = 1,   /* a size is out of range (M, N < 1, K < 32, K % 32 != 0, ...) */
+    W4A8_ERR_MISALIGNED = 2,      /* a pointer is NULL or not 16-byte aligned */
+    W4A8_ERR_CODE_RANGE = 3,      /* w4a8_pack saw a weight code outside [-8, 7] */
+    W4A8_ERR_CUDA = 4,            /* a CUDA runtime call or kernel launch failed */
+    W4A8_ERR_TIMEOUT = 5,         /* a bounded device-side wait ran out (see w4a8_get_device_status) */
+    W4A8_ERR_UNSUPPORTED = 6,     /* the current device is not sm_103, or the shape exceeds a kernel limit */
+    W4A8_ERR_WORKSPACE = 7        /* the workspace passed is NULL or smaller than w4a8_workspace_bytes */
+} w4a8_status;
+
+/* Kernel choice.  The pages switch kernels with the inference phase; here
+ * the phase is read off M (tokens per call). */
+typedef enum {
+    W4A8_PATH_AUTO = 0,     /* w4a8_select_path decides */
+    W4A8_PATH_DECODE = 1,   /* memory-bound GEMV, activations quantised in the kernel; M <= 8 per launch */
+    W4A8_PATH_PREFILL = 2   /* compute-bound tensor-core GEMM (tcgen05) after a quantisation pass */
+} w4a8_path;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *w4a8_status_string(w4a8_status s);
+
+/* Bytes of the packed weight buffer for an N x K layer: N*K/2, or 0 when
+ * N < 1, K < 32 or K % 32 != 0.
+ *
+ * Packed layout (this library's, not the pages'): row-major, row n takes
+ * K/2 bytes; byte j of a row holds weight k = 2j in its low nibble and
+ * k = 2j+1 in its high nibble, each stored as w + 8 (so 0..15 encodes
+ * -8..7).  One 32-weight block is therefore 16 contiguous bytes (one 128-bit
+ * load), a row is K/32 such blocks, and an 8-row by 128-column tile is a
+ * plain 2-D box for the tensor-memory accelerator. */
+size_t w4a8_packed_bytes(int N, int K);
+
+/* Pack int8 weight codes w_codes [N][K] (device, values in [-8, 7]) into
+ * packed_w (device, w4a8_packed_bytes(N, K) bytes).
+ * Synchronises `stream` so it can report W4A8_ERR_CODE_RANGE when any code is
+ * out of range (packed_w then holds those codes' low 4 bits + 8 and must not
+ * be used).  Meant for model load, not for the timed path. */
+w4a8_status w4a8_pack(const int8_t *w_codes, int N, int K, void *packed_w,
+                      cudaStream_t stream);
+
+/* The kernel w4a8_linear would run for this shape (W4A8_PATH_DECODE or
+ * W4A8_PATH_PREFILL): decode for M <= 8, prefill above.  Returns
+ * W4A8_PATH_AUTO (0) for an invalid shape. */
+int w4a8_select_path(int M, int N, int K);
+
+/* Device workspace in bytes that w4a8_linear_ex needs for this shape and
+ * path (W4A8_PATH_AUTO resolves as w4a8_select_path); 0 when none.  The
+ * prefill path keeps the quantised activations there. */
+size_t w4a8_workspace_bytes(int M, int N, int K, int path);
+
+/* y = W4A8 linear of x.
+ *   x       [M][K] fp16, device.
+ *   packed_w       packed weights from w4a8_pack (w4a8_packed_bytes(N, K) bytes).
+ *   scales  [N][K/32] fp16 weight block scales s_w, device, any finite value.
+ *   out     [M][N] fp16, device; must not overlap the inputs.
+ * Requires M >= 1, N >= 1, K >= 32, K % 32 == 0, and x finite (results are
+ * unspecified otherwise).  Asynchronous on `stream`.  When the shape takes
+ * the prefill path this call obtains its workspace with cudaMallocAsync on
+ * `stream` and releases it with cudaFreeAsync after the kernels, so it is
+ * stream-ordered; callers that must not allocate use w4a8_linear_ex. */
+w4a8_status w4a8_linear(const uint16_t *x, const void *packed_w, const uint16_t *scales,
+                        int M, int N, int K, uint16_t *out, cudaStream_t stream);
+
+/* As w4a8_linear, with an explicit path (W4A8_PATH_*) and a caller-owned
+ * device workspace of at least w4a8_workspace_bytes(M, N, K, path) bytes
+ * (may be NULL when that is 0).  Allocates nothing.  The decode path runs
+ * any M by launching once per 8 tokens. */
+w4a8_status w4a8_linear_ex(const uint16_t *x, const void *packed_w, const uint16_t *scales,
+                           int M, int N, int K, uint16_t *out, int path,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Debug: the activation quantiser alone, through the same device routine
+ * the linear kernels use.  codes [M][K] int8 and sx [M][K/32] fp32, device. */
+w4a8_status w4a8_debug_quantize_act(const uint16_t *x, int M, int K, int8_t *codes,
+                                    float *sx, cudaStream_t stream);
+
+/* Debug: the per-block integer dots d[m][n][b] (int32 [M][N][K/32], device)
+ * as the chosen path's kernel computes them (its debug instantiation, which
+ * also stores every block dot).  `out` receives the ordinary fp16 result.
+ * Workspace as for w4a8_linear_ex. */
+w4a8_status w4a8_debug_block_dots(const uint16_t *x, const void *packed_w,
+                                  const uint16_t *scales, int M, int N, int K,
+                                  int32_t *dots, uint16_t *out, int path,
+                                  void *workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
+
+/* Synchronises `stream`, then returns and clears the library's sticky device
+ * status for the current device: W4A8_OK, or W4A8_ERR_TIMEOUT when a bounded
+ * wait inside a kernel ran out since the last call (that kernel's output is
+ * then invalid). */
+w4a8_status w4a8_get_device_status(cudaStream_t stream);
+
+/* Budget, in SM clock cycles, for each bounded device-side wait (default
+ * about two seconds).  For tests of the timeout path; 0 restores the default. */
+w4a8_status w4a8_set_wait_budget(long long cycles);
+
+/* Test hook for the timeout path: launches one CTA that waits, within the
+ * wait budget, on a shared-memory barrier that nothing completes, records
+ * W4A8_ERR_TIMEOUT in the device status and returns. */
+w4a8_status w4a8_debug_wait_timeout(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A8_H */

@@ -1,0 +1,189 @@
+"""Python binding of the GB300 W4A8 block-32 linear (libw4a8.so, C ABI in include/w4a8.h).
+
+Argument marshalling only: every step of the operator runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors; each call is issued on the
+current torch CUDA stream.  The binding never falls back to another
+implementation: if the library is missing or the GPU is not sm_103, calls
+raise.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libw4a8.so")
+
+PATH_AUTO = 0
+PATH_DECODE = 1
+PATH_PREFILL = 2
+
+STATUS = {0: "W4A8_OK", 1: "W4A8_ERR_INVALID_VALUE", 2: "W4A8_ERR_MISALIGNED", 3: "W4A8_ERR_CODE_RANGE",
+          4: "W4A8_ERR_CUDA", 5: "W4A8_ERR_TIMEOUT", 6: "W4A8_ERR_UNSUPPORTED", 7: "W4A8_ERR_WORKSPACE"}
+
+_lib = None
+
+
+class W4A8Error(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        name = STATUS.get(status, str(status))
+        msg = lib().w4a8_status_string(status).decode() if _lib is not None else name
+        super().__init__(f"{what}: {name} ({msg})")
+
+
+def lib():
+    """The loaded C library (loaded on first use; raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                               "(run int4_weight_quantized_gb300.build.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.w4a8_status_string.argtypes = [i]
+        L.w4a8_status_string.restype = ctypes.c_char_p
+        L.w4a8_packed_bytes.argtypes = [i, i]
+        L.w4a8_packed_bytes.restype = sz
+        L.w4a8_pack.argtypes = [P, i, i, P, P]
+        L.w4a8_select_path.argtypes = [i, i, i]
+        L.w4a8_select_path.restype = i
+        L.w4a8_workspace_bytes.argtypes = [i, i, i, i]
+        L.w4a8_workspace_bytes.restype = sz
+        L.w4a8_linear.argtypes = [P, P, P, i, i, i, P, P]
+        L.w4a8_linear_ex.argtypes = [P, P, P, i, i, i, P, i, P, sz, P]
+        L.w4a8_debug_quantize_act.argtypes = [P, i, i, P, P, P]
+        L.w4a8_debug_block_dots.argtypes = [P, P, P, i, i, i, P, P, i, P, sz, P]
+        L.w4a8_get_device_status.argtypes = [P]
+        L.w4a8_set_wait_budget.argtypes = [ctypes.c_longlong]
+        L.w4a8_debug_wait_timeout.argtypes = [P]
+        for f in ("w4a8_pack", "w4a8_linear", "w4a8_linear_ex", "w4a8_debug_quantize_act",
+                  "w4a8_debug_block_dots", "w4a8_get_device_status", "w4a8_set_wait_budget",
+                  "w4a8_debug_wait_timeout"):
+            getattr(L, f).restype = i
+        _lib = L
+    return _lib
+
+
+def _check(status, what):
+    if status != 0:
+        raise W4A8Error(status, what)
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t, dtype, shape, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def packed_bytes(N, K):
+    return lib().w4a8_packed_bytes(N, K)
+
+
+def select_path(M, N, K):
+    return lib().w4a8_select_path(M, N, K)
+
+
+def workspace_bytes(M, N, K, path=PATH_AUTO):
+    return lib().w4a8_workspace_bytes(M, N, K, path)
+
+
+def pack(codes):
+    """int8 weight codes [N][K] in [-8, 7] (CUDA) -> packed uint8 [N, K//2] (synchronises)."""
+    N, K = codes.shape
+    _need(codes, torch.int8, (N, K), "codes")
+    packed = torch.empty((N, K // 2), dtype=torch.uint8, device=codes.device)
+    _check(lib().w4a8_pack(_p(codes), N, K, _p(packed), _stream()), "w4a8_pack")
+    return packed
+
+
+def _linear_shapes(x, packed, scales):
+    M, K = x.shape
+    N = scales.shape[0]
+    _need(x, torch.float16, (M, K), "x")
+    _need(packed, torch.uint8, (N, K // 2), "packed")
+    _need(scales, torch.float16, (N, K // 32), "scales")
+    return M, N, K
+
+
+def make_workspace(M, N, K, path=PATH_AUTO, device="cuda"):
+    """A device workspace of the size the chosen path needs (None when it needs none)."""
+    n = workspace_bytes(M, N, K, path)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def linear(x, packed, scales, out=None, path=PATH_AUTO, workspace=None):
+    """y = W4A8 linear of x: x fp16 [M][K], packed [N][K/2], scales fp16 [N][K/32] -> fp16 [M][N].
+
+    Runs w4a8_linear_ex on the current stream with a caller-side workspace
+    (allocated here from torch's caching allocator when not given)."""
+    M, N, K = _linear_shapes(x, packed, scales)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _need(out, torch.float16, (M, N), "out")
+    need = workspace_bytes(M, N, K, path)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wsb = workspace.numel() if workspace is not None else 0
+    _check(lib().w4a8_linear_ex(_p(x), _p(packed), _p(scales), M, N, K, _p(out), path,
+                                _p(workspace), wsb, _stream()), "w4a8_linear_ex")
+    return out
+
+
+def linear_c(x, packed, scales, out):
+    """The plain C entry point w4a8_linear (automatic path, library-managed workspace)."""
+    M, N, K = _linear_shapes(x, packed, scales)
+    _need(out, torch.float16, (M, N), "out")
+    _check(lib().w4a8_linear(_p(x), _p(packed), _p(scales), M, N, K, _p(out), _stream()), "w4a8_linear")
+    return out
+
+
+def debug_quantize_act(x):
+    """Activation codes int8 [M][K] and scales fp32 [M][K/32] from the library's quantiser."""
+    M, K = x.shape
+    _need(x, torch.float16, (M, K), "x")
+    codes = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    sx = torch.empty((M, K // 32), dtype=torch.float32, device=x.device)
+    _check(lib().w4a8_debug_quantize_act(_p(x), M, K, _p(codes), _p(sx), _stream()),
+           "w4a8_debug_quantize_act")
+    return codes, sx
+
+
+def debug_block_dots(x, packed, scales, path=PATH_AUTO, workspace=None):
+    """(block dots int32 [M][N][K/32], y fp16 [M][N]) from the chosen path's debug kernel."""
+    M, N, K = _linear_shapes(x, packed, scales)
+    dots = torch.empty((M, N, K // 32), dtype=torch.int32, device=x.device)
+    out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    need = workspace_bytes(M, N, K, path)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wsb = workspace.numel() if workspace is not None else 0
+    _check(lib().w4a8_debug_block_dots(_p(x), _p(packed), _p(scales), M, N, K, _p(dots), _p(out), path,
+                                       _p(workspace), wsb, _stream()), "w4a8_debug_block_dots")
+    return dots, out
+
+
+def get_device_status():
+    """Synchronise the current stream and return (and clear) the library's device status code."""
+    return lib().w4a8_get_device_status(_stream())
+
+
+def set_wait_budget(cycles):
+    _check(lib().w4a8_set_wait_budget(int(cycles)), "w4a8_set_wait_budget")
+
+
+def debug_wait_timeout():
+    _check(lib().w4a8_debug_wait_timeout(_stream()), "w4a8_debug_wait_timeout")

@@ -1,0 +1,35 @@
+// kernels.h -- host-side launchers shared between the library's translation units.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#include "../../include/w4a8.h"
+
+namespace w4a8_host {
+
+// Activation quantiser alone, natural layout (debug entry point).
+w4a8_status launch_quant_debug(const uint16_t *x, int M, int K, int8_t *codes, float *sx,
+                               cudaStream_t stream);
+
+// Decode GEMV for any M (one launch per 8 tokens); `dots` non-NULL selects
+// the debug instantiation that also stores every block dot.
+w4a8_status launch_gemv(const uint16_t *x, const void *packed_w, const uint16_t *scales,
+                        int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream);
+
+// Whether the decode GEMV can take this shape (its shared-memory plan fits).
+bool gemv_supported(int M, int N, int K);
+
+// Prefill path: quantisation pass into `workspace`, then the tensor-core GEMM.
+size_t prefill_workspace_bytes(int M, int N, int K);
+w4a8_status launch_prefill(const uint16_t *x, const void *packed_w, const uint16_t *scales,
+                           int M, int N, int K, uint16_t *out, int32_t *dots, void *workspace,
+                           cudaStream_t stream);
+
+// Cycle budget of every bounded device wait, and the device status word of
+// the current device (nullptr if it cannot be resolved).
+long long wait_budget();
+int *device_status_ptr();
+
+}  // namespace w4a8_host

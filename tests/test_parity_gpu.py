@@ -1,0 +1,231 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Integer work (packing, activation codes and scales, per-block dots) must be
+bit-exact; fp16 outputs must meet the tolerance of parity.py.  Inputs come
+from the seeded generators of int4_weight_quantized_gb300.workloads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int4_weight_quantized_gb300 import workloads as wl
+
+from .oracle_pins import load_quant_blocks
+from .parity import assert_fp16_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w4():
+    from int4_weight_quantized_gb300.build import build
+    build()
+    import int4_weight_quantized_gb300 as w4
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return w4
+
+
+def _dev(t):
+    return t.cuda()
+
+
+def _setup(w4, x, codes, scales):
+    xd, cd, sd = _dev(x), _dev(codes), _dev(scales)
+    packed = w4.pack(cd)
+    return xd, packed, sd
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+# ---------------------------------------------------------------- packing
+
+@pytest.mark.parametrize("N,K", [(1, 32), (7, 96), (512, 256), (300, 2048), (8192, 2048)])
+def test_pack_layout(w4, N, K):
+    codes, _ = wl.make_weights(N, K, seed=11 + N, s_lo=0.01, s_hi=0.02)
+    packed = w4.pack(_dev(codes))
+    assert packed.numel() == w4.packed_bytes(N, K)
+    back = oracle.unpack_weights(_np(packed), N, K)
+    assert np.array_equal(back, codes.numpy())
+
+
+def test_pack_rejects_out_of_range_codes(w4):
+    codes = torch.zeros((4, 64), dtype=torch.int8)
+    codes[2, 17] = 9
+    with pytest.raises(w4.W4A8Error) as e:
+        w4.pack(_dev(codes))
+    assert e.value.status == 3
+    codes[2, 17] = -9
+    with pytest.raises(w4.W4A8Error):
+        w4.pack(_dev(codes))
+
+
+# --------------------------------------------------- activation quantiser
+
+def test_quantizer_golden_blocks(w4):
+    blocks = load_quant_blocks()
+    x = np.stack([b[1] for b in blocks])                     # one block per token
+    q, s = w4.debug_quantize_act(_dev(torch.from_numpy(x)))
+    torch.cuda.synchronize()
+    for i, (name, _, qb, sb) in enumerate(blocks):
+        assert np.array_equal(_np(q)[i], qb), name
+        assert int(_np(s)[i].view(np.uint32)[0]) == sb, name
+
+
+@pytest.mark.parametrize("M,K,scale,outliers", [(1, 32, 1.0, 0.0), (3, 256, 1.0, 0.01), (8, 2048, 0.01, 0.01),
+                                                (64, 4096, 300.0, 0.0), (512, 2048, 1.0, 0.01)])
+def test_quantizer_bit_exact(w4, M, K, scale, outliers):
+    x = wl.make_x(M, K, seed=M * 7 + K, outlier_frac=outliers)
+    x = (x.float() * scale).half()
+    if M > 2:
+        x[1] = 0                                            # an all-zero token
+        x[2, 5:37] = torch.tensor(np.arange(1, 33), dtype=torch.int16).view(torch.float16)  # subnormals
+    q, s = w4.debug_quantize_act(_dev(x))
+    qo, so = oracle.quantize_act(x.numpy())
+    assert np.array_equal(_np(q), qo)
+    assert np.array_equal(_np(s).view(np.uint32), so.view(np.uint32))
+
+
+# ---------------------------------------------------------- block dots
+
+DOT_SHAPES = [(1, 1, 32), (1, 37, 96), (2, 100, 1024), (3, 64, 1056), (8, 129, 2048), (5, 257, 4096)]
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("M,N,K", DOT_SHAPES + [(9, 130, 512), (64, 96, 256), (130, 70, 320)])
+def test_block_dots_bit_exact(w4, path, M, N, K):
+    x = wl.make_x(M, K, seed=100 + M, outlier_frac=0.01)
+    codes, scales = wl.make_weights(N, K, seed=200 + N, s_lo=0.002, s_hi=0.01)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    dots, y = w4.debug_block_dots(xd, packed, sd, path=path)
+    q, _ = oracle.quantize_act(x.numpy())
+    ref = oracle.block_dots(q, codes.numpy())
+    assert np.array_equal(_np(dots), ref)
+    assert_fp16_close(_np(y), oracle.linear(x.numpy(), codes.numpy(), scales.numpy()), f"y {M}x{N}x{K}")
+
+
+# ---------------------------------------------------------------- linear
+
+EDGE_SHAPES = ([(M, 67, 160) for M in range(1, 10)] + [(15, 33, 64), (16, 256, 512), (17, 50, 96),
+               (63, 40, 128), (64, 128, 256), (65, 129, 288), (129, 200, 64), (1, 1, 32), (3, 1, 32),
+               (200, 1, 64), (1, 5000, 32), (2, 3, 8192)])
+
+
+@pytest.mark.parametrize("M,N,K", EDGE_SHAPES)
+def test_linear_edge_shapes(w4, M, N, K):
+    x = wl.make_x(M, K, seed=300 + M + K, outlier_frac=0.01)
+    codes, scales = wl.make_weights(N, K, seed=400 + N + K, s_lo=-0.01, s_hi=0.01)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    y = w4.linear(xd, packed, sd)
+    assert_fp16_close(_np(y), oracle.linear(x.numpy(), codes.numpy(), scales.numpy()), f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_linear_zero_inputs(w4, path):
+    M, N, K = 12, 96, 256
+    x = wl.make_x(M, K, seed=5)
+    x[3] = 0
+    x[7, :64] = 0
+    codes, scales = wl.make_weights(N, K, seed=6, s_lo=0.002, s_hi=0.01)
+    codes[10] = 0
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    y = _np(w4.linear(xd, packed, sd, path=path))
+    assert np.all(y[3] == 0) and np.all(y[:, 10] == 0)
+    assert_fp16_close(y, oracle.linear(x.numpy(), codes.numpy(), scales.numpy()))
+    y0 = _np(w4.linear(torch.zeros_like(xd), packed, sd, path=path))
+    assert np.all(y0 == 0)
+
+
+@pytest.mark.parametrize("M", [1, 4, 8, 16, 64])
+def test_paths_agree_on_integer_work(w4, M):
+    """Both kernels compute the same codes and dots; their fp16 outputs differ
+    only by fp32 summation order."""
+    N, K = 300, 1024
+    x = wl.make_x(M, K, seed=M, outlier_frac=0.01)
+    codes, scales = wl.make_weights(N, K, seed=M + 1, s_lo=0.002, s_hi=0.01)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    d1, y1 = w4.debug_block_dots(xd, packed, sd, path=1)
+    d2, y2 = w4.debug_block_dots(xd, packed, sd, path=2)
+    assert torch.equal(d1, d2)
+    assert_fp16_close(_np(y1), _np(y2))
+
+
+def test_c_entry_point_matches_ex(w4):
+    for (M, N, K) in ((1, 512, 256), (300, 256, 512)):
+        x = wl.make_x(M, K, seed=9)
+        codes, scales = wl.make_weights(N, K, seed=10, s_lo=0.002, s_hi=0.01)
+        xd, packed, sd = _setup(w4, x, codes, scales)
+        a = w4.linear(xd, packed, sd)
+        b = torch.empty_like(a)
+        w4.linear_c(xd, packed, sd, b)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b)
+
+
+# ---------------------------------------------- the five workloads at full size
+
+def _sampled_check(w4, lin, seed, weight_set=0, n_cols=96, n_rows=48):
+    """Full-size call on the GPU; the oracle recomputes a sample of output
+    columns (whole W rows, so each sampled output is exact) for a sample of
+    tokens, including the first and last of each."""
+    x, codes, scales = wl.make_linear_inputs(lin, seed, weight_set)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    y = _np(w4.linear(xd, packed, sd))
+    g = np.random.default_rng(seed + weight_set)
+    cols = np.unique(np.concatenate([[0, lin.N - 1], g.choice(lin.N, min(n_cols, lin.N), replace=False)]))
+    rows = np.unique(np.concatenate([[0, lin.M - 1], g.choice(lin.M, min(n_rows, lin.M), replace=False)]))
+    ref = oracle.linear(x.numpy()[rows], codes.numpy()[cols], scales.numpy()[cols])
+    assert_fp16_close(y[np.ix_(rows, cols)], ref, lin.name)
+    return y
+
+
+@pytest.mark.parametrize("wi", range(5))
+def test_workloads_full_size(w4, wi):
+    W = wl.workloads()[wi]
+    for li, lin in enumerate(W.linears):
+        _sampled_check(w4, lin, W.seed + li * 100)
+
+
+def test_tiny_workload_exhaustive(w4):
+    W = wl.workloads()[0]
+    lin = W.linears[0]
+    x, codes, scales = wl.make_linear_inputs(lin, W.seed)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    dots, y = w4.debug_block_dots(xd, packed, sd)
+    q, _ = oracle.quantize_act(x.numpy())
+    assert np.array_equal(_np(dots), oracle.block_dots(q, codes.numpy()))
+    assert_fp16_close(_np(y), oracle.linear(x.numpy(), codes.numpy(), scales.numpy()))
+
+
+# --------------------------------------------------------- failure reporting
+
+def test_bounded_wait_reports_timeout(w4):
+    assert w4.get_device_status() == 0
+    w4.set_wait_budget(200000)
+    try:
+        w4.debug_wait_timeout()
+        assert w4.get_device_status() == 5
+        assert w4.get_device_status() == 0       # cleared by the read
+    finally:
+        w4.set_wait_budget(0)
+    # the context is still usable
+    x = wl.make_x(1, 256, seed=1)
+    codes, scales = wl.make_weights(64, 256, seed=2, s_lo=0.01, s_hi=0.02)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    assert_fp16_close(_np(w4.linear(xd, packed, sd)), oracle.linear(x.numpy(), codes.numpy(), scales.numpy()))
+
+
+def test_workspace_too_small_is_rejected(w4):
+    M, N, K = 64, 128, 256
+    need = w4.workspace_bytes(M, N, K, 2)
+    if need == 0:
+        pytest.skip("prefill path needs no workspace")
+    x = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    codes, scales = wl.make_weights(N, K, seed=3, s_lo=0.01, s_hi=0.02)
+    packed = w4.pack(_dev(codes))
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(w4.W4A8Error) as e:
+        w4.linear(x, packed, _dev(scales), path=2, workspace=ws)
+    assert e.value.status == 7
