@@ -1,19 +1,439 @@
-// gemm.cu -- prefill-phase W4A8 linear.
+// gemm.cu -- prefill-phase W4A8 linear on the 5th-generation tensor cores.
+//
+// Prefill is compute-bound ("Що змінює ML Drift для on-device AI-інференсу на
+// вашому телефоні?", tech.dede.sh, section "Stage-aware оптимізація для
+// великих мовних моделей"), so the block dots run as a dense contraction on
+// tcgen05.  sm_103a has no int8 MMA (tcgen05 kind::i8 is not available on
+// this target), so codes are fed as fp16: every int4 weight (-8..7) and int8
+// activation code (-127..127) is an exact fp16 value, each product is exact in
+// fp32, and every partial sum of one 32-wide block stays below 32*8*127 =
+// 32512 < 2^24, so the fp32 accumulator holds the exact integer block dot.
+//
+// Data flow of one CTA (128 weight rows x 128 tokens, K in stages of 64):
+//   - a quantisation pass (quant.cu) has already written the activation codes
+//     as fp16 [M_pad][K] and the scales s_x as fp32 [K/32][M_pad];
+//   - warp 0 (TMA) loads per stage: the activation tile (128 tokens x 64 k,
+//     128-byte swizzle) and the packed weight tile (128 rows x 32 bytes) into
+//     shared memory, and the stage's s_x rows into a separate ring;
+//   - warps 4-7 expand the int4 weights to fp16 in registers and write them
+//     to tensor memory (tcgen05.st), where the MMA reads them as operand A:
+//     converted weights never touch shared memory;
+//   - warp 1 issues tcgen05.mma (M=128 weight rows, N=128 tokens, K=16) two
+//     per 32-block into one of two TMEM accumulators, overwriting it at the
+//     start of each block;
+//   - warps 8-15 drain each block's exact integer dots from TMEM
+//     (tcgen05.ld) and apply the block scales in fp32 registers:
+//     acc[n][m] += d * (s_w[n,b] * s_x[m,b]); the result is stored as fp16.
+//
+// The contraction order inside each 8-wide group of k is [0,4,1,5,2,6,3,7]
+// on both operands (the cheapest order for unpacking nibbles into fp16
+// pairs); a dot product does not depend on the order of its terms.
+//
+// Every mbarrier wait is bounded (sync.cuh): on timeout the kernel records
+// W4A8_ERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies
+// and MMAs in flight, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "sync.cuh"
+
+namespace {
+
+using namespace w4a8;
+
+constexpr int BM = 128;            // weight rows per CTA: MMA M, TMEM lanes
+constexpr int BN = 128;            // tokens per CTA: MMA N
+constexpr int KS = 64;             // k per pipeline stage (two 32-blocks)
+constexpr int STAGES = 6;
+constexpr int ACT_BYTES = BN * KS * 2;     // 16 KB, fp16 codes, 128B-swizzled rows
+constexpr int W_BYTES = BM * KS / 2;       // 4 KB, packed int4
+constexpr int SX_BYTES = 2 * BN * 4;       // 1 KB, two blocks of s_x
+constexpr int TMEM_COLS = 512;
+constexpr int A_COL0 = 2 * BN;             // after the two accumulators
+constexpr int THREADS = 512;
+
+constexpr int OFF_ACT = 0;
+constexpr int OFF_W = OFF_ACT + STAGES * ACT_BYTES;
+constexpr int OFF_SX = OFF_W + STAGES * W_BYTES;
+constexpr int OFF_BAR = OFF_SX + STAGES * SX_BYTES;
+// barriers: full, conv, empty, sxfull, sxempty (STAGES each), dfull, dempty (2 each), final
+constexpr int NUM_BARS = 5 * STAGES + 4 + 1;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
+
+struct GemmArgs {
+    const uint16_t *sw;      // [N][nb] fp16
+    uint16_t *out;           // [M][N] fp16
+    int32_t *dots;           // debug: [M][N][nb]
+    int *status;
+    long long budget;
+    int M, N, K, nb;
+};
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 ::"r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major rows of 128 bytes, 128-byte
+// swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;                  // leading byte offset (unused with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset
+    d |= (uint64_t)1 << 46;                  // descriptor version
+    d |= (uint64_t)2 << 61;                  // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: fp32 accumulator, fp16 A and B, both K-major.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+#define TC_LD32(taddr, r)                                                                                     \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15," \
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                   \
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),         \
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),     \
+                   "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),  \
+                   "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),  \
+                   "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])                                          \
+                 : "r"(taddr))
+
+#define TC_ST32(taddr, r)                                                                                     \
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
+                 "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"                  \
+                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),    \
+                   "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), \
+                   "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),         \
+                   "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),         \
+                   "r"(r[29]), "r"(r[30]), "r"(r[31])                                                          \
+                 : "memory")
+
+// Two int4 weights (nibbles i and i+4 of a packed word, stored as w+8) to an
+// exact fp16 pair: 0x6400 | u is the fp16 value 1024 + u; subtracting 1032
+// leaves u - 8 = w.
+__device__ __forceinline__ uint32_t nibbles_to_half2(uint32_t word_shifted) {
+    uint32_t t = (word_shifted & 0x000F000Fu) | 0x64006400u;
+    __half2 h = __hsub2(*reinterpret_cast<__half2 *>(&t), __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Bounded wait by every lane of a warp, with one warp-wide outcome (the
+// tcgen05.ld/st that follow are warp-collective).  A failed wait raises the
+// CTA's abort flag; once it is up, waits fail at once.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const GemmArgs &a, volatile uint32_t *abort_flag) {
+    bool ok = (*abort_flag == 0u) && mbar_wait_bounded(bar, parity, a.budget, a.status);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && (threadIdx.x & 31) == 0) *abort_flag = 1u;
+    return ok;
+}
+
+template <bool DEBUG>
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
+                    const __grid_constant__ CUtensorMap tm_sx, GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    uint64_t *full = bars, *conv = bars + STAGES, *empty = bars + 2 * STAGES;
+    uint64_t *sxfull = bars + 3 * STAGES, *sxempty = bars + 4 * STAGES;
+    uint64_t *dfull = bars + 5 * STAGES, *dempty = bars + 5 * STAGES + 2, *finalb = bars + 5 * STAGES + 4;
+    volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC);   // [0] tmem base, [1] abort
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
+    const int nb = a.nb;
+    const int nst = (nb + 1) / 2;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&conv[s], 4);
+            mbar_init(&empty[s], 1);
+            mbar_init(&sxfull[s], 1);
+            mbar_init(&sxempty[s], 8);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&dfull[i], 1);
+            mbar_init(&dempty[i], 8);
+        }
+        mbar_init(finalb, 1);
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32((const void *)&misc[0])), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int s = 0; s < nst; ++s) {
+                const int slot = s % STAGES;
+                const uint32_t ph = (uint32_t)(s / STAGES) & 1u;
+                if (misc[1] || !mbar_wait_bounded(&empty[slot], ph ^ 1u, a.budget, a.status)) { misc[1] = 1; break; }
+                mbar_arrive_expect_tx(&full[slot], ACT_BYTES + W_BYTES);
+                tma_load_2d(sbase + OFF_ACT + slot * ACT_BYTES, &tm_act, s * KS, m0, smem_u32(&full[slot]));
+                tma_load_2d(sbase + OFF_W + slot * W_BYTES, &tm_w, s * (KS / 2), n0, smem_u32(&full[slot]));
+                if (!mbar_wait_bounded(&sxempty[slot], ph ^ 1u, a.budget, a.status)) { misc[1] = 1; issued = s + 1; break; }
+                mbar_arrive_expect_tx(&sxfull[slot], SX_BYTES);
+                tma_load_2d(sbase + OFF_SX + slot * SX_BYTES, &tm_sx, m0, 2 * s, smem_u32(&sxfull[slot]));
+                issued = s + 1;
+            }
+            if (misc[1]) {
+                // let every copy this thread issued land before the CTA exits
+                for (int s = (issued > STAGES ? issued - STAGES : 0); s < issued; ++s) {
+                    const int slot = s % STAGES;
+                    const uint32_t ph = (uint32_t)(s / STAGES) & 1u;
+                    mbar_wait_bounded(&full[slot], ph, a.budget, nullptr);
+                    mbar_wait_bounded(&sxfull[slot], ph, a.budget, nullptr);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            for (int s = 0; s < nst && !misc[1]; ++s) {
+                const int slot = s % STAGES;
+                const uint32_t ph = (uint32_t)(s / STAGES) & 1u;
+                if (!mbar_wait_bounded(&full[slot], ph, a.budget, a.status) ||
+                    !mbar_wait_bounded(&conv[slot], ph, a.budget, a.status)) { misc[1] = 1; break; }
+                tc_fence_after();
+                bool ok = true;
+                for (int j = 0; j < 2; ++j) {
+                    const int b = 2 * s + j;
+                    if (b >= nb) break;
+                    const int buf = b & 1;
+                    if (!mbar_wait_bounded(&dempty[buf], (((uint32_t)b >> 1) & 1u) ^ 1u, a.budget, a.status)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const uint32_t acol = tmem + A_COL0 + slot * 32 + j * 16 + kk * 8;
+                        const uint64_t bdesc = smem_desc_sw128(sbase + OFF_ACT + slot * ACT_BYTES + j * 64 + kk * 32);
+                        tc_mma_ts(tmem + buf * BN, acol, bdesc, kIdesc, (uint32_t)kk);
+                    }
+                    tc_commit(smem_u32(&dfull[buf]));
+                }
+                tc_commit(smem_u32(&empty[slot]));
+                if (!ok) { misc[1] = 1; break; }
+            }
+            // every MMA issued so far has completed once this barrier flips
+            tc_commit(smem_u32(finalb));
+            mbar_wait_bounded(finalb, 0, a.budget, nullptr);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ int4 -> fp16 into TMEM
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        for (int s = 0; s < nst; ++s) {
+            const int slot = s % STAGES;
+            const uint32_t ph = (uint32_t)(s / STAGES) & 1u;
+            if (!warp_wait(&full[slot], ph, a, &misc[1])) break;
+            const uint4 *src = reinterpret_cast<const uint4 *>(smem + OFF_W + slot * W_BYTES + r * 32);
+            const uint4 p0 = src[0], p1 = src[1];
+            const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            uint32_t h[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) h[4 * j + i] = nibbles_to_half2(wd[j] >> (4 * i));
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + A_COL0 + slot * 32;
+            TC_ST32(taddr, h);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&conv[slot]);
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ epilogue
+        const int e = warp - 8;
+        const int q = warp & 3;
+        const int c0 = (e >> 2) * 64;                  // this warp's 64 token columns
+        const int r = q * 32 + lane;
+        const int n = n0 + r;
+        const bool nok = n < a.N;
+        float acc[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+        const uint16_t *swrow = a.sw + (size_t)(nok ? n : 0) * nb;
+        float sw_next = nok ? __half2float(__ushort_as_half(swrow[0])) : 0.0f;
+        for (int b = 0; b < nb; ++b) {
+            const float swf = sw_next;
+            if (b + 1 < nb) sw_next = nok ? __half2float(__ushort_as_half(swrow[b + 1])) : 0.0f;
+            const int s = b >> 1;
+            const int slot = s % STAGES;
+            const uint32_t sph = (uint32_t)(s / STAGES) & 1u;
+            const int buf = b & 1;
+            if (!warp_wait(&dfull[buf], ((uint32_t)b >> 1) & 1u, a, &misc[1])) break;
+            if ((b & 1) == 0 && !warp_wait(&sxfull[slot], sph, a, &misc[1])) break;
+            tc_fence_after();
+            const float *sxp = reinterpret_cast<const float *>(smem + OFF_SX + slot * SX_BYTES) + (b & 1) * BN + c0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t d[32];
+                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c0 + h * 32;
+                TC_LD32(taddr, d);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (h == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&dempty[buf]);
+                }
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 sx4 = *reinterpret_cast<const float4 *>(sxp + h * 32 + i);
+                    const float sxv[4] = {sx4.x, sx4.y, sx4.z, sx4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float dv = __uint_as_float(d[i + u]);
+                        acc[h * 32 + i + u] = fmaf(dv, swf * sxv[u], acc[h * 32 + i + u]);
+                        if (DEBUG) {
+                            const int m = m0 + c0 + h * 32 + i + u;
+                            if (nok && m < a.M) a.dots[((size_t)m * a.N + n) * nb + b] = (int32_t)dv;
+                        }
+                    }
+                }
+            }
+            if ((b & 1) == 1 || b == nb - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sxempty[slot]);
+            }
+        }
+        if (nok && misc[1] == 0u) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const int m = m0 + c0 + i;
+                if (m < a.M) a.out[(size_t)m * a.N + n] = __half_as_ushort(__float2half_rn(acc[i]));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+bool make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *base, uint64_t inner, uint64_t outer,
+                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * (cuuint64_t)esize};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int m_pad(int M) { return (M + BN - 1) / BN * BN; }
+
+template <bool DEBUG>
+w4a8_status launch_t(const CUtensorMap &ta, const CUtensorMap &tw, const CUtensorMap &ts, const GemmArgs &a,
+                     dim3 grid, cudaStream_t stream) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(gemm_w4a8_tc_kernel<DEBUG>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+            cudaSuccess)
+            return W4A8_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    gemm_w4a8_tc_kernel<DEBUG><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tw, ts, a);
+    return w4a8_host::launch_status();
+}
+
+}  // namespace
 
 namespace w4a8_host {
 
 size_t prefill_workspace_bytes(int M, int N, int K) {
-    (void)M; (void)N; (void)K;
-    return 0;
+    (void)N;
+    const size_t mp = (size_t)m_pad(M);
+    return mp * (size_t)K * 2 + (size_t)(K / 32) * mp * 4;
 }
 
 w4a8_status launch_prefill(const uint16_t *x, const void *packed_w, const uint16_t *scales,
                            int M, int N, int K, uint16_t *out, int32_t *dots, void *workspace,
                            cudaStream_t stream) {
-    (void)workspace;
-    return launch_gemv(x, packed_w, scales, M, N, K, out, dots, stream);
+    const int mp = m_pad(M);
+    const int nb = K / 32;
+    uint16_t *q16 = static_cast<uint16_t *>(workspace);
+    float *sx = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + (size_t)mp * K * 2);
+    w4a8_status st = launch_quant_prefill(x, M, K, mp, q16, sx, stream);
+    if (st != W4A8_OK) return st;
+
+    CUtensorMap ta, tw, ts;
+    if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, q16, (uint64_t)K, (uint64_t)mp, KS, BN,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, packed_w, (uint64_t)K / 2, (uint64_t)N, KS / 2, BM,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sx, (uint64_t)mp, (uint64_t)nb, BN, 2,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+        return W4A8_ERR_CUDA;
+
+    GemmArgs a;
+    a.sw = scales;
+    a.out = out;
+    a.dots = dots;
+    a.status = device_status_ptr();
+    a.budget = wait_budget();
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.nb = nb;
+    if (!a.status) return W4A8_ERR_CUDA;
+    dim3 grid((unsigned)((N + BM - 1) / BM), (unsigned)(mp / BN), 1);
+    return dots ? launch_t<true>(ta, tw, ts, a, grid, stream) : launch_t<false>(ta, tw, ts, a, grid, stream);
 }
 
 }  // namespace w4a8_host

@@ -13,6 +13,11 @@ namespace w4a8_host {
 w4a8_status launch_quant_debug(const uint16_t *x, int M, int K, int8_t *codes, float *sx,
                                cudaStream_t stream);
 
+// Prefill quantisation pass: fp16 codes [Mp][K] (k permuted within groups of
+// 8) and scales [K/32][Mp]; rows M..Mp-1 zero.
+w4a8_status launch_quant_prefill(const uint16_t *x, int M, int K, int Mp, uint16_t *q16, float *sx,
+                                 cudaStream_t stream);
+
 // Decode GEMV for any M (one launch per 8 tokens); `dots` non-NULL selects
 // the debug instantiation that also stores every block dot.
 w4a8_status launch_gemv(const uint16_t *x, const void *packed_w, const uint16_t *scales,

@@ -33,9 +33,52 @@ __global__ void __launch_bounds__(256) quant_debug_kernel(const uint16_t *__rest
     }
 }
 
+// Prefill pass: codes as fp16 [Mp][K] for the tensor-core GEMM, with each
+// group of 8 consecutive k stored in the order [0,4,1,5,2,6,3,7] (the order
+// in which the GEMM unpacks nibbles), and scales s_x transposed to
+// [K/32][Mp].  Token rows M..Mp-1 are written as zeros (codes and scales).
+__global__ void __launch_bounds__(256) quant_prefill_kernel(const uint16_t *__restrict__ x, int M, int K, int Mp,
+                                                            uint16_t *__restrict__ q16, float *__restrict__ sx) {
+    const int nb = K / kBlock;
+    const long long items = (long long)Mp * nb * 4;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool act = i < items;
+    int m = 0, b = 0, t = 0;
+    uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+    if (act) {
+        m = (int)(i / (nb * 4));
+        const int rem = (int)(i - (long long)m * nb * 4);
+        b = rem >> 2;
+        t = rem & 3;
+        if (m < M) xv = *reinterpret_cast<const uint4 *>(x + (size_t)m * K + (size_t)b * kBlock + t * 8);
+    }
+    Quant8 r = quant8_group4(xv);
+    if (act) {
+        static constexpr int perm[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = __half_as_ushort(__int2half_rn(r.q[perm[2 * j]]));
+            const uint32_t hi = __half_as_ushort(__int2half_rn(r.q[perm[2 * j + 1]]));
+            w[j] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4 *>(q16 + (size_t)m * K + (size_t)b * kBlock + t * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (t == 0) sx[(size_t)b * Mp + m] = (m < M) ? r.s : 0.0f;
+    }
+}
+
 }  // namespace
 
 namespace w4a8_host {
+
+w4a8_status launch_quant_prefill(const uint16_t *x, int M, int K, int Mp, uint16_t *q16, float *sx,
+                                 cudaStream_t stream) {
+    long long items = (long long)Mp * (K / 32) * 4;
+    unsigned grid = (unsigned)((items + 255) / 256);
+    quant_prefill_kernel<<<grid, 256, 0, stream>>>(x, M, K, Mp, q16, sx);
+    return launch_status();
+}
+
 
 w4a8_status launch_quant_debug(const uint16_t *x, int M, int K, int8_t *codes, float *sx, cudaStream_t stream) {
     long long items = (long long)M * (K / 32) * 4;
