@@ -9,7 +9,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/w4a8.h"
+#include "w4a8.h"
 
 namespace w4a8 {
 

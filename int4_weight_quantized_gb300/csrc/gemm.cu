@@ -48,20 +48,28 @@ using namespace w4a8;
 constexpr int BM = 128;            // weight rows per CTA: MMA M, TMEM lanes
 constexpr int BN = 128;            // tokens per CTA: MMA N
 constexpr int KS = 64;             // k per pipeline stage (two 32-blocks)
-constexpr int STAGES = 6;
+constexpr int S_SM = 8;            // shared-memory stages (activation + packed weight tiles)
+constexpr int S_A = 4;             // TMEM slots of converted weights (operand A)
+constexpr int SXG = 8;             // 32-blocks of s_x per load
+constexpr int S_SX = 4;            // s_x stages (of SXG blocks each)
+constexpr int ND = 3;              // TMEM accumulators (blocks in flight between MMA and epilogue)
 constexpr int ACT_BYTES = BN * KS * 2;     // 16 KB, fp16 codes, 128B-swizzled rows
 constexpr int W_BYTES = BM * KS / 2;       // 4 KB, packed int4
-constexpr int SX_BYTES = 2 * BN * 4;       // 1 KB, two blocks of s_x
+constexpr int SX_BYTES = SXG * BN * 4;     // 4 KB, SXG blocks of s_x
 constexpr int TMEM_COLS = 512;
-constexpr int A_COL0 = 2 * BN;             // after the two accumulators
-constexpr int THREADS = 512;
+constexpr int A_COL0 = ND * BN;            // after the accumulators
+constexpr int EPI_WARPS = 16;         // 4 per TMEM lane quarter, 32 token columns each
+constexpr int CONV_WARP0 = 3;        // warps 3..6 convert weights (one per TMEM lane quarter)
+constexpr int EPI_WARP0 = 7;         // warps 7..22 run the epilogue
+constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
+static_assert(A_COL0 + S_A * 32 <= TMEM_COLS, "TMEM budget");
 
 constexpr int OFF_ACT = 0;
-constexpr int OFF_W = OFF_ACT + STAGES * ACT_BYTES;
-constexpr int OFF_SX = OFF_W + STAGES * W_BYTES;
-constexpr int OFF_BAR = OFF_SX + STAGES * SX_BYTES;
-// barriers: full, conv, empty, sxfull, sxempty (STAGES each), dfull, dempty (2 each), final
-constexpr int NUM_BARS = 5 * STAGES + 4 + 1;
+constexpr int OFF_W = OFF_ACT + S_SM * ACT_BYTES;
+constexpr int OFF_SX = OFF_W + S_SM * W_BYTES;
+constexpr int OFF_BAR = OFF_SX + S_SX * SX_BYTES;
+// barriers: full, empty (S_SM); conv, aempty (S_A); sxfull, sxempty (S_SX); dfull, dempty (ND); final
+constexpr int NUM_BARS = 2 * S_SM + 2 * S_A + 2 * S_SX + 2 * ND + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
 
@@ -156,9 +164,10 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    uint64_t *full = bars, *conv = bars + STAGES, *empty = bars + 2 * STAGES;
-    uint64_t *sxfull = bars + 3 * STAGES, *sxempty = bars + 4 * STAGES;
-    uint64_t *dfull = bars + 5 * STAGES, *dempty = bars + 5 * STAGES + 2, *finalb = bars + 5 * STAGES + 4;
+    uint64_t *full = bars, *empty = full + S_SM;
+    uint64_t *conv = empty + S_SM, *aempty = conv + S_A;
+    uint64_t *sxfull = aempty + S_A, *sxempty = sxfull + S_SX;
+    uint64_t *dfull = sxempty + S_SX, *dempty = dfull + ND, *finalb = dempty + ND;
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC);   // [0] tmem base, [1] abort
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -167,16 +176,21 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
     const int nst = (nb + 1) / 2;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < S_SM; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&conv[s], 4);
             mbar_init(&empty[s], 1);
-            mbar_init(&sxfull[s], 1);
-            mbar_init(&sxempty[s], 8);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int s = 0; s < S_A; ++s) {
+            mbar_init(&conv[s], 4);
+            mbar_init(&aempty[s], 1);
+        }
+        for (int s = 0; s < S_SX; ++s) {
+            mbar_init(&sxfull[s], 1);
+            mbar_init(&sxempty[s], EPI_WARPS);
+        }
+        for (int i = 0; i < ND; ++i) {
             mbar_init(&dfull[i], 1);
-            mbar_init(&dempty[i], 8);
+            mbar_init(&dempty[i], EPI_WARPS);
         }
         mbar_init(finalb, 1);
         misc[1] = 0;
@@ -192,71 +206,78 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ TMA producers
+        // warp 0: activation and weight tiles; warp 2: s_x rows (own ring, so
+        // the main stream never waits for the epilogue)
         if (lane == 0) {
+            const bool main = warp == 0;
+            const int S = main ? S_SM : S_SX;
+            uint64_t *fb = main ? full : sxfull;
+            uint64_t *eb = main ? empty : sxempty;
             int issued = 0;
-            for (int s = 0; s < nst; ++s) {
-                const int slot = s % STAGES;
-                const uint32_t ph = (uint32_t)(s / STAGES) & 1u;
-                if (misc[1] || !mbar_wait_bounded(&empty[slot], ph ^ 1u, a.budget, a.status)) { misc[1] = 1; break; }
-                mbar_arrive_expect_tx(&full[slot], ACT_BYTES + W_BYTES);
-                tma_load_2d(sbase + OFF_ACT + slot * ACT_BYTES, &tm_act, s * KS, m0, smem_u32(&full[slot]));
-                tma_load_2d(sbase + OFF_W + slot * W_BYTES, &tm_w, s * (KS / 2), n0, smem_u32(&full[slot]));
-                if (!mbar_wait_bounded(&sxempty[slot], ph ^ 1u, a.budget, a.status)) { misc[1] = 1; issued = s + 1; break; }
-                mbar_arrive_expect_tx(&sxfull[slot], SX_BYTES);
-                tma_load_2d(sbase + OFF_SX + slot * SX_BYTES, &tm_sx, m0, 2 * s, smem_u32(&sxfull[slot]));
+            const int nloads = main ? nst : (nb + SXG - 1) / SXG;
+            for (int s = 0; s < nloads; ++s) {
+                const int slot = s % S;
+                const uint32_t ph = (uint32_t)(s / S) & 1u;
+                if (misc[1] || !mbar_wait_bounded(&eb[slot], ph ^ 1u, a.budget, a.status)) { misc[1] = 1; break; }
+                if (main) {
+                    mbar_arrive_expect_tx(&fb[slot], ACT_BYTES + W_BYTES);
+                    tma_load_2d(sbase + OFF_ACT + slot * ACT_BYTES, &tm_act, s * KS, m0, smem_u32(&fb[slot]));
+                    tma_load_2d(sbase + OFF_W + slot * W_BYTES, &tm_w, s * (KS / 2), n0, smem_u32(&fb[slot]));
+                } else {
+                    mbar_arrive_expect_tx(&fb[slot], SX_BYTES);
+                    tma_load_2d(sbase + OFF_SX + slot * SX_BYTES, &tm_sx, m0, SXG * s, smem_u32(&fb[slot]));
+                }
                 issued = s + 1;
             }
             if (misc[1]) {
                 // let every copy this thread issued land before the CTA exits
-                for (int s = (issued > STAGES ? issued - STAGES : 0); s < issued; ++s) {
-                    const int slot = s % STAGES;
-                    const uint32_t ph = (uint32_t)(s / STAGES) & 1u;
-                    mbar_wait_bounded(&full[slot], ph, a.budget, nullptr);
-                    mbar_wait_bounded(&sxfull[slot], ph, a.budget, nullptr);
-                }
+                for (int s = (issued > S ? issued - S : 0); s < issued; ++s)
+                    mbar_wait_bounded(&fb[s % S], (uint32_t)(s / S) & 1u, a.budget, nullptr);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             for (int s = 0; s < nst && !misc[1]; ++s) {
-                const int slot = s % STAGES;
-                const uint32_t ph = (uint32_t)(s / STAGES) & 1u;
+                const int slot = s % S_SM, aslot = s % S_A;
+                const uint32_t ph = (uint32_t)(s / S_SM) & 1u, aph = (uint32_t)(s / S_A) & 1u;
                 if (!mbar_wait_bounded(&full[slot], ph, a.budget, a.status) ||
-                    !mbar_wait_bounded(&conv[slot], ph, a.budget, a.status)) { misc[1] = 1; break; }
+                    !mbar_wait_bounded(&conv[aslot], aph, a.budget, a.status)) { misc[1] = 1; break; }
                 tc_fence_after();
                 bool ok = true;
                 for (int j = 0; j < 2; ++j) {
                     const int b = 2 * s + j;
                     if (b >= nb) break;
-                    const int buf = b & 1;
-                    if (!mbar_wait_bounded(&dempty[buf], (((uint32_t)b >> 1) & 1u) ^ 1u, a.budget, a.status)) { ok = false; break; }
+                    const int buf = b % ND;
+                    if (!mbar_wait_bounded(&dempty[buf], ((uint32_t)(b / ND) & 1u) ^ 1u, a.budget, a.status)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t acol = tmem + A_COL0 + slot * 32 + j * 16 + kk * 8;
+                        const uint32_t acol = tmem + A_COL0 + aslot * 32 + j * 16 + kk * 8;
                         const uint64_t bdesc = smem_desc_sw128(sbase + OFF_ACT + slot * ACT_BYTES + j * 64 + kk * 32);
                         tc_mma_ts(tmem + buf * BN, acol, bdesc, kIdesc, (uint32_t)kk);
                     }
                     tc_commit(smem_u32(&dfull[buf]));
                 }
                 tc_commit(smem_u32(&empty[slot]));
+                tc_commit(smem_u32(&aempty[aslot]));
                 if (!ok) { misc[1] = 1; break; }
             }
             // every MMA issued so far has completed once this barrier flips
             tc_commit(smem_u32(finalb));
             mbar_wait_bounded(finalb, 0, a.budget, nullptr);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= CONV_WARP0 && warp < CONV_WARP0 + 4) {
         // ------------------------------------------------------------ int4 -> fp16 into TMEM
         const int q = warp & 3;
         const int r = q * 32 + lane;
         for (int s = 0; s < nst; ++s) {
-            const int slot = s % STAGES;
-            const uint32_t ph = (uint32_t)(s / STAGES) & 1u;
+            const int slot = s % S_SM, aslot = s % S_A;
+            const uint32_t ph = (uint32_t)(s / S_SM) & 1u, aph = (uint32_t)(s / S_A) & 1u;
             if (!warp_wait(&full[slot], ph, a, &misc[1])) break;
+            if (!warp_wait(&aempty[aslot], aph ^ 1u, a, &misc[1])) break;
             const uint4 *src = reinterpret_cast<const uint4 *>(smem + OFF_W + slot * W_BYTES + r * 32);
             const uint4 p0 = src[0], p1 = src[1];
             const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
@@ -265,71 +286,91 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
             for (int j = 0; j < 8; ++j)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) h[4 * j + i] = nibbles_to_half2(wd[j] >> (4 * i));
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + A_COL0 + slot * 32;
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + A_COL0 + aslot * 32;
             TC_ST32(taddr, h);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&conv[slot]);
+            if (lane == 0) mbar_arrive(&conv[aslot]);
         }
-    } else if (warp >= 8) {
+    } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue
-        const int e = warp - 8;
-        const int q = warp & 3;
-        const int c0 = (e >> 2) * 64;                  // this warp's 64 token columns
+        // Per block: one TMEM load of this warp's 32 token columns, release of
+        // the accumulator, then 32 fp32 scale-multiply-adds per thread.  The
+        // barrier of the next block is tested before the arithmetic of this
+        // one, so its latency hides behind the math.
+        const int e = warp - EPI_WARP0;
+        const int q = warp & 3;                        // TMEM lane quarter this warp may access
+        const int c0 = (e >> 2) * 32;                  // this warp's 32 token columns
         const int r = q * 32 + lane;
         const int n = n0 + r;
         const bool nok = n < a.N;
-        float acc[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+        const uint32_t tlane = (uint32_t)(q * 32) << 16;
+        const bool vec_sw = (nb % SXG) == 0;           // rows of s_w start 16-byte aligned
         const uint16_t *swrow = a.sw + (size_t)(nok ? n : 0) * nb;
-        float sw_next = nok ? __half2float(__ushort_as_half(swrow[0])) : 0.0f;
-        for (int b = 0; b < nb; ++b) {
-            const float swf = sw_next;
-            if (b + 1 < nb) sw_next = nok ? __half2float(__ushort_as_half(swrow[b + 1])) : 0.0f;
-            const int s = b >> 1;
-            const int slot = s % STAGES;
-            const uint32_t sph = (uint32_t)(s / STAGES) & 1u;
-            const int buf = b & 1;
-            if (!warp_wait(&dfull[buf], ((uint32_t)b >> 1) & 1u, a, &misc[1])) break;
-            if ((b & 1) == 0 && !warp_wait(&sxfull[slot], sph, a, &misc[1])) break;
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+        auto load_sw = [&](int g, uint4 &v) {
+            if (!nok || g * SXG >= nb) { v = make_uint4(0u, 0u, 0u, 0u); return; }
+            if (vec_sw) { v = __ldg(reinterpret_cast<const uint4 *>(swrow + g * SXG)); return; }
+            auto one = [&](int i) -> uint32_t {
+                const int k = g * SXG + i;
+                return k < nb ? (uint32_t)__ldg(swrow + k) : 0u;
+            };
+            v = make_uint4(one(0) | (one(1) << 16), one(2) | (one(3) << 16), one(4) | (one(5) << 16), one(6) | (one(7) << 16));
+        };
+        uint4 swv, swv_next;
+        load_sw(0, swv_next);
+        bool ok = warp_wait(&dfull[0], 0u, a, &misc[1]);
+        for (int b = 0; ok && b < nb; ++b) {
+            const int g = b / SXG, gi = b % SXG;
+            const int sxslot = g % S_SX;
+            if (gi == 0) {
+                swv = swv_next;
+                load_sw(g + 1, swv_next);
+                if (!warp_wait(&sxfull[sxslot], (uint32_t)(g / S_SX) & 1u, a, &misc[1])) break;
+            }
+            const uint32_t sw_pair = gi < 2 ? swv.x : gi < 4 ? swv.y : gi < 6 ? swv.z : swv.w;
+            const uint32_t swbits = (gi & 1) ? (sw_pair >> 16) : (sw_pair & 0xffffu);
+            const float swf = __half2float(__ushort_as_half((unsigned short)swbits));
+            const int buf = b % ND;
             tc_fence_after();
-            const float *sxp = reinterpret_cast<const float *>(smem + OFF_SX + slot * SX_BYTES) + (b & 1) * BN + c0;
+            uint32_t d[32];
+            TC_LD32(tmem + tlane + buf * BN + c0, d);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dempty[buf]);
+            const bool has_next = b + 1 < nb;
+            const uint32_t next_par = (uint32_t)((b + 1) / ND) & 1u;
+            const bool next_ready = !has_next || mbar_test_wait(&dfull[(b + 1) % ND], next_par);
+            const float *sxp = reinterpret_cast<const float *>(smem + OFF_SX + sxslot * SX_BYTES) + gi * BN + c0;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t d[32];
-                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c0 + h * 32;
-                TC_LD32(taddr, d);
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (h == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&dempty[buf]);
-                }
+            for (int i = 0; i < 32; i += 4) {
+                const float4 sx4 = *reinterpret_cast<const float4 *>(sxp + i);
+                const float sxv[4] = {sx4.x, sx4.y, sx4.z, sx4.w};
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 sx4 = *reinterpret_cast<const float4 *>(sxp + h * 32 + i);
-                    const float sxv[4] = {sx4.x, sx4.y, sx4.z, sx4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float dv = __uint_as_float(d[i + u]);
-                        acc[h * 32 + i + u] = fmaf(dv, swf * sxv[u], acc[h * 32 + i + u]);
-                        if (DEBUG) {
-                            const int m = m0 + c0 + h * 32 + i + u;
-                            if (nok && m < a.M) a.dots[((size_t)m * a.N + n) * nb + b] = (int32_t)dv;
-                        }
+                for (int u = 0; u < 4; ++u) {
+                    const float dv = __uint_as_float(d[i + u]);
+                    acc[i + u] = fmaf(dv, swf * sxv[u], acc[i + u]);
+                    if (DEBUG) {
+                        const int m = m0 + c0 + i + u;
+                        if (nok && m < a.M) a.dots[((size_t)m * a.N + n) * nb + b] = (int32_t)dv;
                     }
                 }
             }
-            if ((b & 1) == 1 || b == nb - 1) {
+            if (gi == SXG - 1 || b == nb - 1) {
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sxempty[slot]);
+                if (lane == 0) mbar_arrive(&sxempty[sxslot]);
             }
+            if (has_next && !__all_sync(0xffffffffu, next_ready))
+                ok = warp_wait(&dfull[(b + 1) % ND], next_par, a, &misc[1]);
         }
         if (nok && misc[1] == 0u) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
+            for (int i = 0; i < 32; ++i) {
                 const int m = m0 + c0 + i;
                 if (m < a.M) a.out[(size_t)m * a.N + n] = __half_as_ushort(__float2half_rn(acc[i]));
             }
@@ -417,7 +458,7 @@ w4a8_status launch_prefill(const uint16_t *x, const void *packed_w, const uint16
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, packed_w, (uint64_t)K / 2, (uint64_t)N, KS / 2, BM,
                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sx, (uint64_t)mp, (uint64_t)nb, BN, 2,
+        !make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sx, (uint64_t)mp, (uint64_t)nb, BN, SXG,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4A8_ERR_CUDA;
 

@@ -5,7 +5,7 @@
 #include <stdint.h>
 #include <cuda_runtime.h>
 
-#include "../../include/w4a8.h"
+#include "w4a8.h"
 
 namespace w4a8_host {
 
