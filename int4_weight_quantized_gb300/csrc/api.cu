@@ -122,7 +122,7 @@ size_t w4a8_packed_bytes(int N, int K) {
 
 int w4a8_select_path(int M, int N, int K) {
     if (!shape_ok(M, N, K)) return W4A8_PATH_AUTO;
-    if (M <= 8 && gemv_supported(M, N, K)) return W4A8_PATH_DECODE;
+    if (M <= 8 && (gemv_stream_supported(M, N, K) || gemv_supported(M, N, K))) return W4A8_PATH_DECODE;
     return W4A8_PATH_PREFILL;
 }
 
@@ -147,6 +147,7 @@ static w4a8_status run_linear(const uint16_t *x, const void *packed_w, const uin
     if (path == W4A8_PATH_AUTO) path = w4a8_select_path(M, N, K);
     cudaGetLastError();
     if (path == W4A8_PATH_DECODE) {
+        if (gemv_stream_supported(M, N, K)) return launch_gemv_stream(x, packed_w, scales, M, N, K, out, dots, stream);
         if (!gemv_supported(M < 8 ? M : 8, N, K)) return W4A8_ERR_UNSUPPORTED;
         return launch_gemv(x, packed_w, scales, M, N, K, out, dots, stream);
     }

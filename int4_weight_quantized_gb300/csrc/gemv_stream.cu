@@ -1,0 +1,415 @@
+// gemv_stream.cu -- decode-phase W4A8 linear that streams each CTA's weight
+// rows through a shared-memory ring with bulk asynchronous copies.
+//
+// Decode is memory-bound: the time is the weight stream ("Що змінює ML Drift
+// для on-device AI-інференсу на вашому телефоні?", tech.dede.sh, section
+// "Stage-aware оптимізація для великих мовних моделей").  This kernel keeps
+// that stream busy:
+//   - each CTA owns a contiguous range of output rows; since the packed
+//     layout is row-major, the range is one contiguous byte range, copied in
+//     chunks of CR whole rows (weights and their fp16 block scales) by one
+//     producer warp with cp.async.bulk into an S-deep ring;
+//   - the first S chunks are requested before the kernel waits for the
+//     previous kernel on the stream (programmatic dependent launch), so a
+//     call's weight reads overlap the tail of the call before it; only the
+//     activations and the output depend on earlier work;
+//   - activations are then quantised in the kernel (the pages' in-kernel
+//     activation quantisation) into shared memory, and every lane keeps the
+//     codes of its K blocks (l, l+32, l+64, ...) in registers;
+//   - one warp computes one whole row at a time: lane l reads its BPL
+//     16-byte blocks of the row from the ring (32 int4 weights each), does
+//     8 dp4a per block and token and one fp32 multiply-add with s_w * s_x,
+//     and the 32 lanes are summed with shuffles; the warp then stores the
+//     row's outputs itself, so no cross-warp reduction is needed.
+// Packed weights are stored as w + 8: dp4a of the unsigned nibbles gives
+// d + 8*sum(q), and starting the integer accumulator at 0x4B400000 - 8*sum(q)
+// leaves the float 1.5*2^23 + d, from which d follows exactly by one fp32
+// subtraction.
+#include "common.cuh"
+#include "kernels.h"
+#include "sync.cuh"
+
+namespace {
+
+using namespace w4a8;
+
+constexpr int CWARPS = 8;                   // consumer warps
+constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
+constexpr int STAGES = 8;
+constexpr int STAGE_TARGET = 32768;         // weight bytes per chunk (about)
+constexpr int MAX_SMEM = 110 * 1024;        // leaves room for a second CTA (next launch) per SM
+
+struct StreamArgs {
+    const uint16_t *x;
+    const uint8_t *pw;
+    const uint16_t *sw;
+    uint16_t *out;
+    int32_t *dots;       // debug instantiation only
+    int *status;
+    long long budget;
+    int M, N, K, nb;
+    int rows_per_cta;    // R
+    int cr;              // rows per chunk
+    int sw_bulk;         // scales copied with the weights (nb % 8 == 0)
+    size_t stage_bytes;  // weights + scales per stage, 16-byte multiple
+    int nslots;          // ring slots (<= STAGES)
+};
+
+struct Layout {
+    size_t ring, act_codes, act_sx, act_cb, part, bars, total;
+};
+
+__host__ __device__ inline Layout layout(int MT, int nb, size_t stage_bytes, int nslots) {
+    Layout L;
+    size_t o = 0;
+    L.ring = o;
+    o += (size_t)nslots * stage_bytes;
+    L.act_codes = o;
+    o += (size_t)MT * nb * 32;
+    L.act_sx = o;
+    o += (size_t)MT * nb * 4;
+    L.act_cb = o;
+    o += (size_t)MT * nb * 4;
+    L.part = o;
+    o = (o + 15) & ~(size_t)15;
+    L.bars = o;
+    o += 2 * STAGES * 8;
+    L.total = o;
+    return L;
+}
+
+// Bulk copy global -> shared, marked evict-first in L2: weights are read once
+// per call, and should not push the (re-used) activations out of L2.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(CWARPS * 32) : "memory"); }
+
+template <int MT, int BPL, bool DEBUG>
+__global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
+    constexpr int RG = MT <= 2 ? 4 : (MT <= 4 ? 2 : 1);    // rows reduced together per warp
+    extern __shared__ __align__(16) uint8_t smem[];
+    const Layout L = layout(MT, a.nb, a.stage_bytes, a.nslots);
+    const int NS = a.nslots;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + NS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = blockIdx.x * a.rows_per_cta;
+    const int r1 = min(a.N, r0 + a.rows_per_cta);
+    const int nrows = max(0, r1 - r0);
+    const int nchunks = (nrows + a.cr - 1) / a.cr;
+    const size_t row_bytes = (size_t)a.K / 2;
+    const size_t w_stage = (size_t)a.cr * row_bytes;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CWARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == CWARPS) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int issued = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % NS;
+                const uint32_t ph = (uint32_t)(c / NS) & 1u;
+                if (!mbar_wait_bounded(&empty[s], ph ^ 1u, a.budget, a.status)) break;
+                const int rows = min(a.cr, nrows - c * a.cr);
+                const int rr = r0 + c * a.cr;
+                const uint32_t wbytes = (uint32_t)(rows * row_bytes);
+                const uint32_t sbytes = a.sw_bulk ? (uint32_t)(rows * a.nb * 2) : 0u;
+                const uint32_t dst = smem_u32(smem + L.ring + (size_t)s * a.stage_bytes);
+                mbar_arrive_expect_tx(&full[s], wbytes + sbytes);
+                bulk_g2s(dst, a.pw + (size_t)rr * row_bytes, wbytes, smem_u32(&full[s]), pol);
+                if (sbytes) bulk_g2s(dst + (uint32_t)w_stage, a.sw + (size_t)rr * a.nb, sbytes, smem_u32(&full[s]), pol);
+                if (c == NS - 1 || c == nchunks - 1) pdl_launch_dependents();
+                issued = c + 1;
+            }
+            if (nchunks == 0) pdl_launch_dependents();
+            // the CTA must not retire while its copies are still landing
+            for (int c = (issued > NS ? issued - NS : 0); c < issued; ++c)
+                mbar_wait_bounded(&full[c % NS], (uint32_t)(c / NS) & 1u, a.budget, nullptr);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // Activations may be produced by the previous kernel on the stream.
+    pdl_wait();
+    uint32_t *codes = reinterpret_cast<uint32_t *>(smem + L.act_codes);
+    float *sxs = reinterpret_cast<float *>(smem + L.act_sx);
+    int *cbs = reinterpret_cast<int *>(smem + L.act_cb);
+    const int tid = threadIdx.x;
+    {
+        const int items = MT * a.nb * 4;
+        for (int base = 0; base < items; base += CWARPS * 32) {
+            const int i = base + tid;
+            const bool act = i < items;
+            int m = 0, b = 0, t = 0;
+            uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+            if (act) {
+                m = i / (a.nb * 4);
+                const int rem = i - m * a.nb * 4;
+                b = rem >> 2;
+                t = rem & 3;
+                if (m < a.M) xv = *reinterpret_cast<const uint4 *>(a.x + (size_t)m * a.K + (size_t)b * kBlock + t * 8);
+            }
+            Quant8 r = quant8_group4(xv);
+            if (act) {
+                uint32_t *cw = codes + ((size_t)m * a.nb + b) * 8;
+                cw[2 * t] = pack_bytes4(r.q[0], r.q[2], r.q[4], r.q[6]);
+                cw[2 * t + 1] = pack_bytes4(r.q[1], r.q[3], r.q[5], r.q[7]);
+                if (t == 0) {
+                    sxs[m * a.nb + b] = r.s;
+                    cbs[m * a.nb + b] = kMagicBits - 8 * r.sum;
+                }
+            }
+        }
+    }
+    consumer_sync();
+
+    // this lane's K blocks (lane + 32 j) and their activation codes, in registers
+    uint32_t qa[MT][BPL][8];
+    float sxr[MT][BPL];
+    int cbr[MT][BPL];
+#pragma unroll
+    for (int j = 0; j < BPL; ++j) {
+        const int b = lane + 32 * j;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (b < a.nb) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(codes + ((size_t)m * a.nb + b) * 8);
+                const uint4 c0 = src[0], c1 = src[1];
+                qa[m][j][0] = c0.x; qa[m][j][1] = c0.y; qa[m][j][2] = c0.z; qa[m][j][3] = c0.w;
+                qa[m][j][4] = c1.x; qa[m][j][5] = c1.y; qa[m][j][6] = c1.z; qa[m][j][7] = c1.w;
+                sxr[m][j] = sxs[m * a.nb + b];
+                cbr[m][j] = cbs[m * a.nb + b];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) qa[m][j][i] = 0u;
+                sxr[m][j] = 0.0f;
+                cbr[m][j] = kMagicBits;
+            }
+        }
+    }
+
+    const bool reuse = nchunks > NS;         // ring slots are refilled: release them
+    for (int c = 0; c < nchunks; ++c) {
+        const int s = c % NS;
+        const uint32_t ph = (uint32_t)(c / NS) & 1u;
+        bool ok = mbar_wait_bounded(&full[s], ph, a.budget, a.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return;
+        const uint8_t *wst = smem + L.ring + (size_t)s * a.stage_bytes;
+        const uint16_t *sst = reinterpret_cast<const uint16_t *>(wst + w_stage);
+        const int rows = min(a.cr, nrows - c * a.cr);
+        // RG consecutive rows per warp at a time: their shuffle reductions
+        // are independent and overlap
+        for (int rb = warp * RG; rb < rows; rb += CWARPS * RG) {
+            float v[RG][MT];
+#pragma unroll
+            for (int g = 0; g < RG; ++g)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) v[g][m] = 0.0f;
+#pragma unroll
+            for (int g = 0; g < RG; ++g) {
+                const int rr = rb + g;
+                if (rr >= rows) break;
+                const int n = r0 + c * a.cr + rr;
+#pragma unroll
+                for (int j = 0; j < BPL; ++j) {
+                    const int b = lane + 32 * j;
+                    if (b < a.nb) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(wst + (size_t)rr * row_bytes + (size_t)b * 16);
+                        const uint16_t swh = a.sw_bulk ? sst[(size_t)rr * a.nb + b] : __ldg(a.sw + (size_t)n * a.nb + b);
+                        const float swf = __half2float(__ushort_as_half(swh));
+                        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+                        uint32_t lo[4], hi[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            lo[i] = nib_even(w4[i]);
+                            hi[i] = nib_odd(w4[i]);
+                        }
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            int d = cbr[m][j];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                d = dp4a_us(lo[i], qa[m][j][2 * i], d);
+                                d = dp4a_us(hi[i], qa[m][j][2 * i + 1], d);
+                            }
+                            if (DEBUG && m < a.M) a.dots[((size_t)m * a.N + n) * a.nb + b] = d - kMagicBits;
+                            v[g][m] = fmaf(__int_as_float(d) - kMagic, swf * sxr[m][j], v[g][m]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int g = 0; g < RG; ++g)
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) v[g][m] += __shfl_xor_sync(0xffffffffu, v[g][m], o);
+            // lane g*MT + m stores row rb+g, token m
+            float mine = 0.0f;
+#pragma unroll
+            for (int g = 0; g < RG; ++g)
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+                    if (lane == g * MT + m) mine = v[g][m];
+            const int g = lane / MT, m = lane - (lane / MT) * MT;
+            if (lane < RG * MT && rb + g < rows && m < a.M)
+                a.out[(size_t)m * a.N + r0 + c * a.cr + rb + g] = __half_as_ushort(__float2half_rn(mine));
+        }
+        if (reuse) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+    }
+}
+
+struct Plan {
+    int MT, BPL, R, cr, sw_bulk, nslots;
+    size_t stage_bytes, smem;
+    int grid;
+    bool ok;
+};
+
+constexpr int kSMs = 152;
+
+Plan make_plan(int M, int N, int K) {
+    Plan p{};
+    const int nb = K / 32;
+    p.MT = M < 8 ? M : 8;
+    p.BPL = (nb + 31) / 32;
+    p.ok = (p.BPL == 1 || p.BPL == 2 || p.BPL == 4 || p.BPL == 8) && p.MT * p.BPL <= 8;
+    const size_t row_bytes = (size_t)K / 2;
+    p.sw_bulk = (nb % 8) == 0;
+    p.R = (N + kSMs - 1) / kSMs;
+    p.grid = (N + p.R - 1) / p.R;
+    // about four chunks per CTA, each a whole number of rows
+    const size_t cta_bytes = (size_t)p.R * row_bytes;
+    size_t target = (cta_bytes + 3) / 4;
+    if (target < (size_t)STAGE_TARGET) target = STAGE_TARGET;
+    p.cr = (int)(target / row_bytes);
+    if (p.cr < 1) p.cr = 1;
+    if (p.cr > p.R) p.cr = p.R;
+    auto size_up = [&]() {
+        p.stage_bytes = ((size_t)p.cr * row_bytes + (p.sw_bulk ? (size_t)p.cr * nb * 2 : 0) + 15) & ~(size_t)15;
+        const int nch = (p.R + p.cr - 1) / p.cr;
+        p.nslots = nch < STAGES ? nch : STAGES;
+        p.smem = layout(p.MT, nb, p.stage_bytes, p.nslots).total;
+    };
+    size_up();
+    while (p.smem > (size_t)MAX_SMEM && p.cr > 1) {      // shrink chunks until the ring fits
+        p.cr = (p.cr + 1) / 2;
+        size_up();
+    }
+    if (p.smem > (size_t)MAX_SMEM) p.ok = false;
+    return p;
+}
+
+template <int MT, int BPL, bool DEBUG>
+w4a8_status launch_t(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
+    auto kern = gemv_stream_kernel<MT, BPL, DEBUG>;
+    static int attr_done[64] = {};   // per device: the opt-in shared-memory limit is set once
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W4A8_ERR_CUDA;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SMEM) != cudaSuccess)
+            return W4A8_ERR_CUDA;
+        attr_done[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A8_ERR_CUDA;
+    }
+    return w4a8_host::launch_status();
+}
+
+template <bool DEBUG>
+w4a8_status dispatch(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
+    switch (p.MT * 16 + p.BPL) {
+        case 1 * 16 + 1: return launch_t<1, 1, DEBUG>(p, a, stream);
+        case 1 * 16 + 2: return launch_t<1, 2, DEBUG>(p, a, stream);
+        case 1 * 16 + 4: return launch_t<1, 4, DEBUG>(p, a, stream);
+        case 1 * 16 + 8: return launch_t<1, 8, DEBUG>(p, a, stream);
+        case 2 * 16 + 1: return launch_t<2, 1, DEBUG>(p, a, stream);
+        case 2 * 16 + 2: return launch_t<2, 2, DEBUG>(p, a, stream);
+        case 2 * 16 + 4: return launch_t<2, 4, DEBUG>(p, a, stream);
+        case 3 * 16 + 1: return launch_t<3, 1, DEBUG>(p, a, stream);
+        case 3 * 16 + 2: return launch_t<3, 2, DEBUG>(p, a, stream);
+        case 4 * 16 + 1: return launch_t<4, 1, DEBUG>(p, a, stream);
+        case 4 * 16 + 2: return launch_t<4, 2, DEBUG>(p, a, stream);
+        case 5 * 16 + 1: return launch_t<5, 1, DEBUG>(p, a, stream);
+        case 6 * 16 + 1: return launch_t<6, 1, DEBUG>(p, a, stream);
+        case 7 * 16 + 1: return launch_t<7, 1, DEBUG>(p, a, stream);
+        case 8 * 16 + 1: return launch_t<8, 1, DEBUG>(p, a, stream);
+        default: return W4A8_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+namespace w4a8_host {
+
+bool gemv_stream_supported(int M, int N, int K) { return make_plan(M < 8 ? M : 8, N, K).ok; }
+
+w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const uint16_t *scales,
+                               int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream) {
+    int *status = device_status_ptr();
+    if (!status) return W4A8_ERR_CUDA;
+    for (int m0 = 0; m0 < M; m0 += 8) {
+        const int mc = (M - m0) < 8 ? (M - m0) : 8;
+        Plan p = make_plan(mc, N, K);
+        if (!p.ok) return W4A8_ERR_UNSUPPORTED;
+        StreamArgs a;
+        a.x = x + (size_t)m0 * K;
+        a.pw = static_cast<const uint8_t *>(packed_w);
+        a.sw = scales;
+        a.out = out + (size_t)m0 * N;
+        a.dots = dots ? dots + (size_t)m0 * N * (K / 32) : nullptr;
+        a.status = status;
+        a.budget = wait_budget();
+        a.M = mc;
+        a.N = N;
+        a.K = K;
+        a.nb = K / 32;
+        a.rows_per_cta = p.R;
+        a.cr = p.cr;
+        a.sw_bulk = p.sw_bulk;
+        a.stage_bytes = p.stage_bytes;
+        a.nslots = p.nslots;
+        w4a8_status st = dots ? dispatch<true>(p, a, stream) : dispatch<false>(p, a, stream);
+        if (st != W4A8_OK) return st;
+    }
+    return W4A8_OK;
+}
+
+}  // namespace w4a8_host

@@ -26,6 +26,13 @@ w4a8_status launch_gemv(const uint16_t *x, const void *packed_w, const uint16_t 
 // Whether the decode GEMV can take this shape (its shared-memory plan fits).
 bool gemv_supported(int M, int N, int K);
 
+// Decode GEMV that streams weight rows through a shared-memory ring with
+// bulk copies (programmatic dependent launch); supported when K/32 blocks
+// form 1, 2, 4 or 8 slices of 32 and the shared-memory plan fits.
+bool gemv_stream_supported(int M, int N, int K);
+w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const uint16_t *scales,
+                               int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream);
+
 // Prefill path: quantisation pass into `workspace`, then the tensor-core GEMM.
 size_t prefill_workspace_bytes(int M, int N, int K);
 w4a8_status launch_prefill(const uint16_t *x, const void *packed_w, const uint16_t *scales,
