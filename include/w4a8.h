@@ -133,6 +133,27 @@ w4a8_status w4a8_debug_block_dots(const uint16_t *x, const void *packed_w,
                                   void *workspace, size_t workspace_bytes,
                                   cudaStream_t stream);
 
+/* Prefill (tensor-core) linear that allocates nothing, for callers that
+ * cannot allocate device memory: code running in a CUDA-graph node or host
+ * callback, plugins of engines that own every allocation, or real-time loops
+ * where an allocator call (which may synchronise, or fail under memory
+ * pressure) is not allowed.  The pages have no counterpart to this entry
+ * point; it exists for such callers only.
+ *   Arguments, layouts and results are those of w4a8_linear_ex with
+ *   W4A8_PATH_PREFILL.  The quantised activations go to a fixed 16 MiB
+ *   scratch array compiled into the library; every GPU that loads the library
+ *   keeps that array until the process exits.  A shape whose scratch need
+ *   (w4a8_workspace_bytes(M, N, K, W4A8_PATH_PREFILL)) exceeds 16 MiB is
+ *   rejected with W4A8_ERR_WORKSPACE before anything is launched.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls share the one array: calls whose work overlaps on the GPU (on
+ *   different streams, or from different host threads) race and must be
+ *   ordered by the caller.  Each call overwrites all of the scratch it reads,
+ *   so nothing from an earlier call leaks into a later one. */
+w4a8_status w4a8_linear_prefill_noalloc(const uint16_t *x, const void *packed_w, const uint16_t *scales,
+                                        int M, int N, int K, uint16_t *out, cudaStream_t stream);
+
 /* Synchronises `stream`, then returns and clears the library's sticky device
  * status for the current device: W4A8_OK, or W4A8_ERR_TIMEOUT when a bounded
  * wait inside a kernel ran out since the last call (that kernel's output is

@@ -54,10 +54,11 @@ def lib():
         L.w4a8_linear_ex.argtypes = [P, P, P, i, i, i, P, i, P, sz, P]
         L.w4a8_debug_quantize_act.argtypes = [P, i, i, P, P, P]
         L.w4a8_debug_block_dots.argtypes = [P, P, P, i, i, i, P, P, i, P, sz, P]
+        L.w4a8_linear_prefill_noalloc.argtypes = [P, P, P, i, i, i, P, P]
         L.w4a8_get_device_status.argtypes = [P]
         L.w4a8_set_wait_budget.argtypes = [ctypes.c_longlong]
         L.w4a8_debug_wait_timeout.argtypes = [P]
-        for f in ("w4a8_pack", "w4a8_linear", "w4a8_linear_ex", "w4a8_debug_quantize_act",
+        for f in ("w4a8_pack", "w4a8_linear", "w4a8_linear_ex", "w4a8_linear_prefill_noalloc", "w4a8_debug_quantize_act",
                   "w4a8_debug_block_dots", "w4a8_get_device_status", "w4a8_set_wait_budget",
                   "w4a8_debug_wait_timeout"):
             getattr(L, f).restype = i
@@ -148,6 +149,17 @@ def linear_c(x, packed, scales, out):
     M, N, K = _linear_shapes(x, packed, scales)
     _need(out, torch.float16, (M, N), "out")
     _check(lib().w4a8_linear(_p(x), _p(packed), _p(scales), M, N, K, _p(out), _stream()), "w4a8_linear")
+    return out
+
+
+def linear_prefill_noalloc(x, packed, scales, out):
+    """Prefill linear through w4a8_linear_prefill_noalloc: no device allocation
+    anywhere (the library's fixed scratch array holds the quantised
+    activations).  For callers that cannot allocate; calls must not overlap."""
+    M, N, K = _linear_shapes(x, packed, scales)
+    _need(out, torch.float16, (M, N), "out")
+    _check(lib().w4a8_linear_prefill_noalloc(_p(x), _p(packed), _p(scales), M, N, K, _p(out), _stream()),
+           "w4a8_linear_prefill_noalloc")
     return out
 
 
