@@ -264,11 +264,14 @@ def main():
     value = ws * bytes_step * args.steps / (ms * 1e-3) / 1e9
     per_launch_s = ms * 1e-3 / (args.steps * cps)
     hbm, bf16, bf16_sus, peak_src = peaks()
-    gemv_files = ["int4_weight_quantized_gb300/csrc/gemv.cu", "int4_weight_quantized_gb300/csrc/common.cuh"]
+    gemv_files = ["int4_weight_quantized_gb300/csrc/gemv_stream.cu", "int4_weight_quantized_gb300/csrc/common.cuh",
+                  "int4_weight_quantized_gb300/csrc/sync.cuh"]
     achieved = lin.bytes / per_launch_s / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-            "traffic": traffic_for("gemv_decode_ffn_up", gemv_files), "peak_source": peak_src,
-            "kernel": "gemv_kernel<1,4,false>", "algorithmic_bytes_per_launch": lin.bytes}
+            "traffic": traffic_for("gemv_stream_decode_ffn_up", gemv_files), "peak_source": peak_src,
+            "kernel": "gemv_stream_kernel<1,2,false>", "algorithmic_bytes_per_launch": lin.bytes,
+            "launch_time_us": per_launch_s * 1e6,
+            "note": "launch time = timed region / launches (every launch in the step is this kernel)"}
 
     # ---- end to end through the C entry point with pinned host buffers
     e2e_steps = max(3, min(args.steps, 50))
@@ -362,7 +365,49 @@ def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src):
                              "frac": tops / bf16, "peak_source": peak_src,
                              "note": "contraction runs on fp16 tensor cores (exact for int4 x int8 codes); "
                                      "peak is the dense fp16/bf16 tensor rate"}})
+    res.append(run_decoder_layers(w4, wl, dev, stream, hbm, peak_src))
     return res
+
+
+def run_decoder_layers(w4, wl, dev, stream, hbm, peak_src, steps=20):
+    """One decode step over 26 decoder layers x 7 linears (M=1), captured as a
+    CUDA graph of 182 launches; effective HBM GB/s over the step."""
+    import torch
+    W = [w for w in wl.workloads() if w.name == "decoder_layers_m1_26x7"][0]
+    layers = W.extra["layers"]
+    linears = []
+    with torch.cuda.stream(stream):
+        for layer in range(layers):
+            for li, lin in enumerate(W.linears):
+                seed = W.seed + 100 * layer + li
+                c, s = wl.make_weights_on(dev, lin.N, lin.K, seed, lin.s_lo, lin.s_hi)
+                x = wl.make_x(lin.M, lin.K, seed, lin.outlier_frac).to(dev)
+                linears.append((x, w4.pack(c), s, torch.empty((lin.M, lin.N), dtype=torch.float16, device=dev)))
+                del c
+        step_bytes = layers * sum(l.bytes for l in W.linears)
+
+        def step():
+            for x, p, s, o in linears:
+                w4.linear(x, p, s, out=o, path=w4.PATH_DECODE)
+        step()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+        e1.synchronize()
+    per_step = e0.elapsed_time(e1) * 1e-3 / steps
+    gbs = step_bytes / per_step / 1e9
+    return {"workload": W.name, "value": gbs, "unit": "GB/s", "us_per_decode_step": per_step * 1e6,
+            "launches_per_step": len(linears), "bytes_per_step": step_bytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "peak_source": peak_src}}
 
 
 if __name__ == "__main__":

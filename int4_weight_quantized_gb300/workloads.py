@@ -2,8 +2,9 @@
 
 This module only draws random numbers: it holds none of the operator's
 arithmetic, and both the CUDA path and the CPU oracle take their inputs from
-it.  Every draw uses a CPU ``torch.Generator`` so that the same seed gives the
-same tensors on any host.
+it.  Draws use a CPU ``torch.Generator`` so that the same seed gives the same
+tensors on any host; only make_weights_on (for the 876 MB decoder-layer
+benchmark, never compared with the oracle) draws on the GPU.
 
 Shapes follow the pages' LLM workload: prefill length 512 and one-token decode
 with 4-bit weights in blocks of 32 ("Що змінює ML Drift для on-device
@@ -28,6 +29,18 @@ def make_weights(N: int, K: int, seed: int, s_lo: float, s_hi: float):
     g = torch.Generator().manual_seed(seed)
     codes = torch.randint(-8, 8, (N, K), generator=g, dtype=torch.int8)
     scales = (torch.rand((N, K // BLOCK), generator=g, dtype=torch.float32)
+              * (s_hi - s_lo) + s_lo).to(torch.float16)
+    return codes, scales
+
+
+def make_weights_on(device, N: int, K: int, seed: int, s_lo: float, s_hi: float):
+    """As make_weights, drawn by a seeded generator on `device` (for workloads
+    too large to draw on the host; the values differ from make_weights')."""
+    if K % BLOCK:
+        raise ValueError("K must be a multiple of 32")
+    g = torch.Generator(device=device).manual_seed(seed)
+    codes = torch.randint(-8, 8, (N, K), generator=g, dtype=torch.int8, device=device)
+    scales = (torch.rand((N, K // BLOCK), generator=g, dtype=torch.float32, device=device)
               * (s_hi - s_lo) + s_lo).to(torch.float16)
     return codes, scales
 
