@@ -47,22 +47,25 @@ using namespace w4a8;
 
 constexpr int BM = 128;            // weight rows per CTA: MMA M, TMEM lanes
 constexpr int BN = 128;            // tokens per CTA: MMA N
-constexpr int KS = 64;             // k per pipeline stage (two 32-blocks)
-constexpr int S_SM = 8;            // shared-memory stages (activation + packed weight tiles)
-constexpr int S_A = 4;             // TMEM slots of converted weights (operand A)
+constexpr int KS = 128;            // k per pipeline stage (four 32-blocks)
+constexpr int BPS = KS / 32;       // blocks per stage
+constexpr int S_SM = 4;            // shared-memory stages (activation + packed weight tiles)
+constexpr int S_A = 2;             // TMEM slots of converted weights (operand A), BPS*16 columns each
 constexpr int SXG = 8;             // 32-blocks of s_x per load
 constexpr int S_SX = 4;            // s_x stages (of SXG blocks each)
 constexpr int ND = 3;              // TMEM accumulators (blocks in flight between MMA and epilogue)
-constexpr int ACT_BYTES = BN * KS * 2;     // 16 KB, fp16 codes, 128B-swizzled rows
-constexpr int W_BYTES = BM * KS / 2;       // 4 KB, packed int4
-constexpr int SX_BYTES = SXG * BN * 4;     // 4 KB, SXG blocks of s_x
+constexpr int ACT_SUB = BN * 64 * 2;        // 16 KB: 128 tokens x 64 k, one 128-byte-swizzle atom column
+constexpr int ACT_BYTES = ACT_SUB * (KS / 64);
+constexpr int W_BYTES = BM * KS / 2;        // 8 KB, packed int4
+constexpr int SX_BYTES = SXG * BN * 4;      // 4 KB, SXG blocks of s_x
 constexpr int TMEM_COLS = 512;
-constexpr int A_COL0 = ND * BN;            // after the accumulators
-constexpr int EPI_WARPS = 16;         // 4 per TMEM lane quarter, 32 token columns each
+constexpr int A_COL0 = ND * BN;             // after the accumulators
+constexpr int A_COLS = BPS * 16;            // fp16 pairs of one stage's weights
+constexpr int EPI_WARPS = 8;          // 2 per TMEM lane quarter, 64 token columns each
 constexpr int CONV_WARP0 = 3;        // warps 3..6 convert weights (one per TMEM lane quarter)
-constexpr int EPI_WARP0 = 7;         // warps 7..22 run the epilogue
+constexpr int EPI_WARP0 = 7;         // warps 7..14 run the epilogue
 constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
-static_assert(A_COL0 + S_A * 32 <= TMEM_COLS, "TMEM budget");
+static_assert(A_COL0 + S_A * A_COLS <= TMEM_COLS, "TMEM budget");
 
 constexpr int OFF_ACT = 0;
 constexpr int OFF_W = OFF_ACT + S_SM * ACT_BYTES;
@@ -173,7 +176,7 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
     const int nb = a.nb;
-    const int nst = (nb + 1) / 2;
+    const int nst = (nb + BPS - 1) / BPS;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S_SM; ++s) {
@@ -223,7 +226,10 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
                 if (misc[1] || !mbar_wait_bounded(&eb[slot], ph ^ 1u, a.budget, a.status)) { misc[1] = 1; break; }
                 if (main) {
                     mbar_arrive_expect_tx(&fb[slot], ACT_BYTES + W_BYTES);
-                    tma_load_2d(sbase + OFF_ACT + slot * ACT_BYTES, &tm_act, s * KS, m0, smem_u32(&fb[slot]));
+#pragma unroll
+                    for (int u = 0; u < KS / 64; ++u)
+                        tma_load_2d(sbase + OFF_ACT + slot * ACT_BYTES + u * ACT_SUB, &tm_act, s * KS + u * 64, m0,
+                                    smem_u32(&fb[slot]));
                     tma_load_2d(sbase + OFF_W + slot * W_BYTES, &tm_w, s * (KS / 2), n0, smem_u32(&fb[slot]));
                 } else {
                     mbar_arrive_expect_tx(&fb[slot], SX_BYTES);
@@ -239,27 +245,37 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Barrier tests are issued together and only the unready ones are
+        // waited on, so their latencies overlap.
         if (lane == 0) {
+            int buf = 0;
+            uint32_t dpar = 1u;          // "previous phase" parity: the first use of each accumulator is free
             for (int s = 0; s < nst && !misc[1]; ++s) {
                 const int slot = s % S_SM, aslot = s % S_A;
                 const uint32_t ph = (uint32_t)(s / S_SM) & 1u, aph = (uint32_t)(s / S_A) & 1u;
-                if (!mbar_wait_bounded(&full[slot], ph, a.budget, a.status) ||
-                    !mbar_wait_bounded(&conv[aslot], aph, a.budget, a.status)) { misc[1] = 1; break; }
+                const bool f_ok = mbar_test_wait(&full[slot], ph);
+                const bool c_ok = mbar_test_wait(&conv[aslot], aph);
+                if ((!f_ok && !mbar_wait_bounded(&full[slot], ph, a.budget, a.status)) ||
+                    (!c_ok && !mbar_wait_bounded(&conv[aslot], aph, a.budget, a.status))) { misc[1] = 1; break; }
                 tc_fence_after();
                 bool ok = true;
-                for (int j = 0; j < 2; ++j) {
-                    const int b = 2 * s + j;
+                for (int j = 0; j < BPS; ++j) {
+                    const int b = BPS * s + j;
                     if (b >= nb) break;
-                    const int buf = b % ND;
-                    if (!mbar_wait_bounded(&dempty[buf], ((uint32_t)(b / ND) & 1u) ^ 1u, a.budget, a.status)) { ok = false; break; }
+                    if (!mbar_test_wait(&dempty[buf], dpar) && !mbar_wait_bounded(&dempty[buf], dpar, a.budget, a.status)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t acol = tmem + A_COL0 + aslot * 32 + j * 16 + kk * 8;
-                        const uint64_t bdesc = smem_desc_sw128(sbase + OFF_ACT + slot * ACT_BYTES + j * 64 + kk * 32);
+                        const uint32_t acol = tmem + A_COL0 + aslot * A_COLS + j * 16 + kk * 8;
+                        const uint64_t bdesc = smem_desc_sw128(sbase + OFF_ACT + slot * ACT_BYTES + (j >> 1) * ACT_SUB +
+                                                               (j & 1) * 64 + kk * 32);
                         tc_mma_ts(tmem + buf * BN, acol, bdesc, kIdesc, (uint32_t)kk);
                     }
                     tc_commit(smem_u32(&dfull[buf]));
+                    if (++buf == ND) { buf = 0; dpar ^= 1u; }
                 }
                 tc_commit(smem_u32(&empty[slot]));
                 tc_commit(smem_u32(&aempty[aslot]));
@@ -276,19 +292,24 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
         for (int s = 0; s < nst; ++s) {
             const int slot = s % S_SM, aslot = s % S_A;
             const uint32_t ph = (uint32_t)(s / S_SM) & 1u, aph = (uint32_t)(s / S_A) & 1u;
-            if (!warp_wait(&full[slot], ph, a, &misc[1])) break;
-            if (!warp_wait(&aempty[aslot], aph ^ 1u, a, &misc[1])) break;
-            const uint4 *src = reinterpret_cast<const uint4 *>(smem + OFF_W + slot * W_BYTES + r * 32);
-            const uint4 p0 = src[0], p1 = src[1];
-            const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-            uint32_t h[32];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) h[4 * j + i] = nibbles_to_half2(wd[j] >> (4 * i));
+            const bool f_ok = mbar_test_wait(&full[slot], ph);
+            const bool e_ok = mbar_test_wait(&aempty[aslot], aph ^ 1u);
+            if (!__all_sync(0xffffffffu, f_ok) && !warp_wait(&full[slot], ph, a, &misc[1])) break;
+            if (!__all_sync(0xffffffffu, e_ok) && !warp_wait(&aempty[aslot], aph ^ 1u, a, &misc[1])) break;
             tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + A_COL0 + aslot * 32;
-            TC_ST32(taddr, h);
+            const uint4 *src = reinterpret_cast<const uint4 *>(smem + OFF_W + slot * W_BYTES + r * (KS / 2));
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + A_COL0 + aslot * A_COLS;
+#pragma unroll
+            for (int hh = 0; hh < KS / 64; ++hh) {
+                const uint4 p0 = src[2 * hh], p1 = src[2 * hh + 1];
+                const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                uint32_t h[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) h[4 * j + i] = nibbles_to_half2(wd[j] >> (4 * i));
+                TC_ST32(taddr + hh * 32, h);
+            }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
@@ -296,22 +317,22 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
         }
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue
-        // Per block: one TMEM load of this warp's 32 token columns, release of
-        // the accumulator, then 32 fp32 scale-multiply-adds per thread.  The
-        // barrier of the next block is tested before the arithmetic of this
-        // one, so its latency hides behind the math.
+        // Per block: two TMEM loads of 32 token columns each (this warp owns
+        // 64), 64 fp32 scale-multiply-adds per thread, release of the
+        // accumulator after the second load.  Ring positions advance by
+        // counters, not divisions.
         const int e = warp - EPI_WARP0;
         const int q = warp & 3;                        // TMEM lane quarter this warp may access
-        const int c0 = (e >> 2) * 32;                  // this warp's 32 token columns
+        const int c0 = (e >> 2) * 64;                  // this warp's 64 token columns
         const int r = q * 32 + lane;
         const int n = n0 + r;
         const bool nok = n < a.N;
-        const uint32_t tlane = (uint32_t)(q * 32) << 16;
+        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
         const bool vec_sw = (nb % SXG) == 0;           // rows of s_w start 16-byte aligned
         const uint16_t *swrow = a.sw + (size_t)(nok ? n : 0) * nb;
-        float acc[32];
+        float acc[64];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
         auto load_sw = [&](int g, uint4 &v) {
             if (!nok || g * SXG >= nb) { v = make_uint4(0u, 0u, 0u, 0u); return; }
             if (vec_sw) { v = __ldg(reinterpret_cast<const uint4 *>(swrow + g * SXG)); return; }
@@ -321,43 +342,43 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
             };
             v = make_uint4(one(0) | (one(1) << 16), one(2) | (one(3) << 16), one(4) | (one(5) << 16), one(6) | (one(7) << 16));
         };
-        uint4 swv, swv_next;
+        uint4 swv = make_uint4(0u, 0u, 0u, 0u), swv_next;
         load_sw(0, swv_next);
-        bool ok = warp_wait(&dfull[0], 0u, a, &misc[1]);
-        for (int b = 0; ok && b < nb; ++b) {
-            const int g = b / SXG, gi = b % SXG;
-            const int sxslot = g % S_SX;
+        int buf = 0, g = 0, gi = 0, sxslot = 0;
+        uint32_t dpar = 0u, sxpar = 0u;
+        for (int b = 0; b < nb; ++b) {
             if (gi == 0) {
                 swv = swv_next;
                 load_sw(g + 1, swv_next);
-                if (!warp_wait(&sxfull[sxslot], (uint32_t)(g / S_SX) & 1u, a, &misc[1])) break;
+                if (!mbar_test_wait(&sxfull[sxslot], sxpar) && !warp_wait(&sxfull[sxslot], sxpar, a, &misc[1])) break;
             }
             const uint32_t sw_pair = gi < 2 ? swv.x : gi < 4 ? swv.y : gi < 6 ? swv.z : swv.w;
-            const uint32_t swbits = (gi & 1) ? (sw_pair >> 16) : (sw_pair & 0xffffu);
-            const float swf = __half2float(__ushort_as_half((unsigned short)swbits));
-            const int buf = b % ND;
+            const float swf = __half2float(__ushort_as_half((unsigned short)((gi & 1) ? (sw_pair >> 16) : (sw_pair & 0xffffu))));
+            if (!mbar_test_wait(&dfull[buf], dpar) && !warp_wait(&dfull[buf], dpar, a, &misc[1])) break;
             tc_fence_after();
-            uint32_t d[32];
-            TC_LD32(tmem + tlane + buf * BN + c0, d);
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&dempty[buf]);
-            const bool has_next = b + 1 < nb;
-            const uint32_t next_par = (uint32_t)((b + 1) / ND) & 1u;
-            const bool next_ready = !has_next || mbar_test_wait(&dfull[(b + 1) % ND], next_par);
             const float *sxp = reinterpret_cast<const float *>(smem + OFF_SX + sxslot * SX_BYTES) + gi * BN + c0;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                const float4 sx4 = *reinterpret_cast<const float4 *>(sxp + i);
-                const float sxv[4] = {sx4.x, sx4.y, sx4.z, sx4.w};
+            for (int h = 0; h < 2; ++h) {
+                uint32_t d[32];
+                TC_LD32(tbase + (uint32_t)(buf * BN + h * 32), d);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (h == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&dempty[buf]);
+                }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float dv = __uint_as_float(d[i + u]);
-                    acc[i + u] = fmaf(dv, swf * sxv[u], acc[i + u]);
-                    if (DEBUG) {
-                        const int m = m0 + c0 + i + u;
-                        if (nok && m < a.M) a.dots[((size_t)m * a.N + n) * nb + b] = (int32_t)dv;
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 sx4 = *reinterpret_cast<const float4 *>(sxp + h * 32 + i);
+                    const float sxv[4] = {sx4.x, sx4.y, sx4.z, sx4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float dv = __uint_as_float(d[i + u]);
+                        acc[h * 32 + i + u] = fmaf(dv, swf * sxv[u], acc[h * 32 + i + u]);
+                        if (DEBUG) {
+                            const int m = m0 + c0 + h * 32 + i + u;
+                            if (nok && m < a.M) a.dots[((size_t)m * a.N + n) * nb + b] = (int32_t)dv;
+                        }
                     }
                 }
             }
@@ -365,12 +386,16 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sxempty[sxslot]);
             }
-            if (has_next && !__all_sync(0xffffffffu, next_ready))
-                ok = warp_wait(&dfull[(b + 1) % ND], next_par, a, &misc[1]);
+            if (++buf == ND) { buf = 0; dpar ^= 1u; }
+            if (++gi == SXG) {
+                gi = 0;
+                ++g;
+                if (++sxslot == S_SX) { sxslot = 0; sxpar ^= 1u; }
+            }
         }
         if (nok && misc[1] == 0u) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 64; ++i) {
                 const int m = m0 + c0 + i;
                 if (m < a.M) a.out[(size_t)m * a.N + n] = __half_as_ushort(__float2half_rn(acc[i]));
             }
@@ -454,7 +479,7 @@ w4a8_status launch_prefill(const uint16_t *x, const void *packed_w, const uint16
     if (st != W4A8_OK) return st;
 
     CUtensorMap ta, tw, ts;
-    if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, q16, (uint64_t)K, (uint64_t)mp, KS, BN,
+    if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, q16, (uint64_t)K, (uint64_t)mp, 64, BN,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, packed_w, (uint64_t)K / 2, (uint64_t)N, KS / 2, BM,
                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
