@@ -143,6 +143,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(ms, ws, device):
+    """Slowest rank's time (ms); every rank returns the same value."""
+    if ws <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank, ms, ws):
+    """Whole-job GB/s: every rank moved bytes_per_rank in the slowest rank's time (weak scaling)."""
+    return ws * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def oracle_inputs(lin, seed):
     from int4_weight_quantized_gb300 import workloads as wl
     x, codes, scales = wl.make_linear_inputs(lin, seed, 0)
@@ -253,15 +270,10 @@ def main():
             e1.record(stream)
             e1.synchronize()
         torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.barrier()
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     ms_step = ms / args.steps
     bytes_step = lin.bytes * cps
-    value = ws * bytes_step * args.steps / (ms * 1e-3) / 1e9
+    value = job_throughput(bytes_step * args.steps, ms, ws)
     per_launch_s = ms * 1e-3 / (args.steps * cps)
     hbm, bf16, bf16_sus, peak_src = peaks()
     gemv_files = ["int4_weight_quantized_gb300/csrc/gemv_stream.cu", "int4_weight_quantized_gb300/csrc/common.cuh",
@@ -366,7 +378,54 @@ def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src):
                              "note": "contraction runs on fp16 tensor cores (exact for int4 x int8 codes); "
                                      "peak is the dense fp16/bf16 tensor rate"}})
     res.append(run_decoder_layers(w4, wl, dev, stream, hbm, peak_src))
+    res.append(run_sweep(w4, wl, dev, stream, hbm, bf16, peak_src))
     return res
+
+
+def run_sweep(w4, wl, dev, stream, hbm, bf16, peak_src, sets=5, reps=20):
+    """The K/N shape sweep under the automatic stage-aware dispatch: per shape,
+    a CUDA graph of calls over `sets` rotating weight sets (> L2 in total)."""
+    import torch
+    W = [w for w in wl.workloads() if w.name == "shape_sweep"][0]
+    rows = []
+    with torch.cuda.stream(stream):
+        for li, lin in enumerate(W.linears):
+            ws = []
+            for i in range(sets):
+                c, s = wl.make_weights_on(dev, lin.N, lin.K, W.seed + 10 * li + i, lin.s_lo, lin.s_hi)
+                ws.append((w4.pack(c), s))
+                del c
+            x = wl.make_x(lin.M, lin.K, W.seed + li, lin.outlier_frac).to(dev)
+            out = torch.empty((lin.M, lin.N), dtype=torch.float16, device=dev)
+            path = w4.select_path(lin.M, lin.N, lin.K)
+            wsp = w4.make_workspace(lin.M, lin.N, lin.K, path, dev)
+
+            def calls():
+                for p, s in ws:
+                    w4.linear(x, p, s, out=out, path=path, workspace=wsp)
+            calls()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                calls()
+            for _ in range(3):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            per_call = e0.elapsed_time(e1) * 1e-3 / (reps * sets)
+            gbs = lin.bytes / per_call / 1e9
+            tops = lin.ops / per_call / 1e12
+            rows.append({"M": lin.M, "K": lin.K, "N": lin.N,
+                         "path": "decode" if path == w4.PATH_DECODE else "prefill",
+                         "us_per_call": per_call * 1e6, "GB_s": gbs, "TOPS": tops,
+                         "frac_hbm": gbs / hbm, "frac_fp16_tensor": tops / bf16})
+            del ws
+    return {"workload": W.name, "rows": rows, "peak_source": peak_src,
+            "note": "decode rows are judged on GB/s against HBM, prefill rows on TOPS against the fp16 tensor peak"}
 
 
 def run_decoder_layers(w4, wl, dev, stream, hbm, peak_src, steps=20):
