@@ -9,19 +9,22 @@
 // fp32, and every partial sum of one 32-wide block stays below 32*8*127 =
 // 32512 < 2^24, so the fp32 accumulator holds the exact integer block dot.
 //
-// Data flow of one CTA (128 weight rows x 128 tokens, K in stages of 64):
+// Data flow of one CTA (128 weight rows x 128 tokens, K in stages of 64 =
+// two 32-blocks):
 //   - a quantisation pass (quant.cu) has already written the activation codes
 //     as fp16 [M_pad][K] and the scales s_x as fp32 [K/32][M_pad];
-//   - warp 0 (TMA) loads per stage: the activation tile (128 tokens x 64 k,
-//     128-byte swizzle) and the packed weight tile (128 rows x 32 bytes) into
-//     shared memory, and the stage's s_x rows into a separate ring;
-//   - warps 4-7 expand the int4 weights to fp16 in registers and write them
-//     to tensor memory (tcgen05.st), where the MMA reads them as operand A:
-//     converted weights never touch shared memory;
-//   - warp 1 issues tcgen05.mma (M=128 weight rows, N=128 tokens, K=16) two
-//     per 32-block into one of two TMEM accumulators, overwriting it at the
-//     start of each block;
-//   - warps 8-15 drain each block's exact integer dots from TMEM
+//   - warp 0 (TMA) loads per stage the activation tile (128 tokens x 64 k,
+//     128-byte swizzle) and the packed weight tile (128 rows x 32 bytes);
+//     warp 2 loads s_x rows into a ring of their own;
+//   - warps 3-6 expand the int4 weights to fp16 and write them into shared
+//     memory in the same 128-byte-swizzled K-major layout, where the MMA
+//     reads them as operand A;
+//   - warp 1 issues tcgen05.mma (M=128 weight rows, N=128 tokens, K=16), two
+//     per 32-block, each block into its own TMEM accumulator; the four
+//     accumulators (all 512 columns) form two pairs, and the MMA and
+//     epilogue hand a pair back and forth with one signal each way, so the
+//     per-handshake cost is paid once per 64 k;
+//   - warps 7-14 drain each block's exact integer dots from TMEM
 //     (tcgen05.ld) and apply the block scales in fp32 registers:
 //     acc[n][m] += d * (s_w[n,b] * s_x[m,b]); the result is stored as fp16.
 //
@@ -47,32 +50,27 @@ using namespace w4a8;
 
 constexpr int BM = 128;            // weight rows per CTA: MMA M, TMEM lanes
 constexpr int BN = 128;            // tokens per CTA: MMA N
-constexpr int KS = 128;            // k per pipeline stage (four 32-blocks)
-constexpr int BPS = KS / 32;       // blocks per stage
-constexpr int S_SM = 4;            // shared-memory stages (activation + packed weight tiles)
-constexpr int S_A = 2;             // TMEM slots of converted weights (operand A), BPS*16 columns each
+constexpr int KS = 64;             // k per pipeline stage: two 32-blocks, one accumulator pair
+constexpr int S_SM = 4;            // shared-memory stages
 constexpr int SXG = 8;             // 32-blocks of s_x per load
 constexpr int S_SX = 4;            // s_x stages (of SXG blocks each)
-constexpr int ND = 3;              // TMEM accumulators (blocks in flight between MMA and epilogue)
-constexpr int ACT_SUB = BN * 64 * 2;        // 16 KB: 128 tokens x 64 k, one 128-byte-swizzle atom column
-constexpr int ACT_BYTES = ACT_SUB * (KS / 64);
-constexpr int W_BYTES = BM * KS / 2;        // 8 KB, packed int4
+constexpr int NP = 2;              // accumulator pairs in TMEM (2 x 2 x 128 columns = all 512)
+constexpr int TILE = 128 * 128;    // bytes of one 128-row x 64-k fp16 tile (one 128-byte-swizzle atom column)
+constexpr int W_BYTES = BM * KS / 2;        // 4 KB, packed int4 of one stage
 constexpr int SX_BYTES = SXG * BN * 4;      // 4 KB, SXG blocks of s_x
 constexpr int TMEM_COLS = 512;
-constexpr int A_COL0 = ND * BN;             // after the accumulators
-constexpr int A_COLS = BPS * 16;            // fp16 pairs of one stage's weights
 constexpr int EPI_WARPS = 8;          // 2 per TMEM lane quarter, 64 token columns each
-constexpr int CONV_WARP0 = 3;        // warps 3..6 convert weights (one per TMEM lane quarter)
+constexpr int CONV_WARP0 = 3;        // warps 3..6 convert weights (32 rows each)
 constexpr int EPI_WARP0 = 7;         // warps 7..14 run the epilogue
 constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
-static_assert(A_COL0 + S_A * A_COLS <= TMEM_COLS, "TMEM budget");
 
-constexpr int OFF_ACT = 0;
-constexpr int OFF_W = OFF_ACT + S_SM * ACT_BYTES;
+constexpr int OFF_ACT = 0;                          // S_SM activation tiles (TMA, swizzled)
+constexpr int OFF_A = OFF_ACT + S_SM * TILE;        // S_SM fp16 weight tiles (converter, swizzled)
+constexpr int OFF_W = OFF_A + S_SM * TILE;          // S_SM packed weight tiles (TMA)
 constexpr int OFF_SX = OFF_W + S_SM * W_BYTES;
 constexpr int OFF_BAR = OFF_SX + S_SX * SX_BYTES;
-// barriers: full, empty (S_SM); conv, aempty (S_A); sxfull, sxempty (S_SX); dfull, dempty (ND); final
-constexpr int NUM_BARS = 2 * S_SM + 2 * S_A + 2 * S_SX + 2 * ND + 1;
+// barriers: full, conv, empty (S_SM); sxfull, sxempty (S_SX); dfull, dempty (NP); final
+constexpr int NUM_BARS = 3 * S_SM + 2 * S_SX + 2 * NP + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack to align the base to 1024
 
@@ -97,11 +95,17 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, fp16 inputs, fp32 accumulate.
-__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+// D[tmem] (+)= A[smem] * B[smem]^T, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-                 ::"r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the
+// async proxy (the tensor cores read operand tiles through it).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor: K-major rows of 128 bytes, 128-byte
@@ -128,16 +132,6 @@ constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t
                    "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),  \
                    "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])                                          \
                  : "r"(taddr))
-
-#define TC_ST32(taddr, r)                                                                                     \
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
-                 "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"                  \
-                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),    \
-                   "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), \
-                   "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),         \
-                   "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),         \
-                   "r"(r[29]), "r"(r[30]), "r"(r[31])                                                          \
-                 : "memory")
 
 // Two int4 weights (nibbles i and i+4 of a packed word, stored as w+8) to an
 // exact fp16 pair: 0x6400 | u is the fp16 value 1024 + u; subtracting 1032
@@ -167,31 +161,27 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    uint64_t *full = bars, *empty = full + S_SM;
-    uint64_t *conv = empty + S_SM, *aempty = conv + S_A;
-    uint64_t *sxfull = aempty + S_A, *sxempty = sxfull + S_SX;
-    uint64_t *dfull = sxempty + S_SX, *dempty = dfull + ND, *finalb = dempty + ND;
+    uint64_t *full = bars, *conv = full + S_SM, *empty = conv + S_SM;
+    uint64_t *sxfull = empty + S_SM, *sxempty = sxfull + S_SX;
+    uint64_t *dfull = sxempty + S_SX, *dempty = dfull + NP, *finalb = dempty + NP;
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC);   // [0] tmem base, [1] abort
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
     const int nb = a.nb;
-    const int nst = (nb + BPS - 1) / BPS;
+    const int nst = (nb + 1) / 2;               // stages = accumulator pairs
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S_SM; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int s = 0; s < S_A; ++s) {
             mbar_init(&conv[s], 4);
-            mbar_init(&aempty[s], 1);
+            mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < S_SX; ++s) {
             mbar_init(&sxfull[s], 1);
             mbar_init(&sxempty[s], EPI_WARPS);
         }
-        for (int i = 0; i < ND; ++i) {
+        for (int i = 0; i < NP; ++i) {
             mbar_init(&dfull[i], 1);
             mbar_init(&dempty[i], EPI_WARPS);
         }
@@ -211,8 +201,8 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ TMA producers
-        // warp 0: activation and weight tiles; warp 2: s_x rows (own ring, so
-        // the main stream never waits for the epilogue)
+        // warp 0: activation and packed-weight tiles; warp 2: s_x rows (own
+        // ring, so the main stream never waits for the epilogue)
         if (lane == 0) {
             const bool main = warp == 0;
             const int S = main ? S_SM : S_SX;
@@ -223,13 +213,13 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
             for (int s = 0; s < nloads; ++s) {
                 const int slot = s % S;
                 const uint32_t ph = (uint32_t)(s / S) & 1u;
-                if (misc[1] || !mbar_wait_bounded(&eb[slot], ph ^ 1u, a.budget, a.status)) { misc[1] = 1; break; }
+                if (misc[1] || !(mbar_test_wait(&eb[slot], ph ^ 1u) || mbar_wait_bounded(&eb[slot], ph ^ 1u, a.budget, a.status))) {
+                    misc[1] = 1;
+                    break;
+                }
                 if (main) {
-                    mbar_arrive_expect_tx(&fb[slot], ACT_BYTES + W_BYTES);
-#pragma unroll
-                    for (int u = 0; u < KS / 64; ++u)
-                        tma_load_2d(sbase + OFF_ACT + slot * ACT_BYTES + u * ACT_SUB, &tm_act, s * KS + u * 64, m0,
-                                    smem_u32(&fb[slot]));
+                    mbar_arrive_expect_tx(&fb[slot], TILE + W_BYTES);
+                    tma_load_2d(sbase + OFF_ACT + slot * TILE, &tm_act, s * KS, m0, smem_u32(&fb[slot]));
                     tma_load_2d(sbase + OFF_W + slot * W_BYTES, &tm_w, s * (KS / 2), n0, smem_u32(&fb[slot]));
                 } else {
                     mbar_arrive_expect_tx(&fb[slot], SX_BYTES);
@@ -245,82 +235,73 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // Barrier tests are issued together and only the unready ones are
-        // waited on, so their latencies overlap.
+        // One stage = one accumulator pair: two 32-blocks, each two K=16 MMAs
+        // into its own accumulator; one completion signal per pair.
         if (lane == 0) {
-            int buf = 0;
-            uint32_t dpar = 1u;          // "previous phase" parity: the first use of each accumulator is free
             for (int s = 0; s < nst && !misc[1]; ++s) {
-                const int slot = s % S_SM, aslot = s % S_A;
-                const uint32_t ph = (uint32_t)(s / S_SM) & 1u, aph = (uint32_t)(s / S_A) & 1u;
+                const int slot = s % S_SM, pr = s % NP;
+                const uint32_t ph = (uint32_t)(s / S_SM) & 1u, pp = (uint32_t)(s / NP) & 1u;
                 const bool f_ok = mbar_test_wait(&full[slot], ph);
-                const bool c_ok = mbar_test_wait(&conv[aslot], aph);
+                const bool c_ok = mbar_test_wait(&conv[slot], ph);
+                const bool d_ok = mbar_test_wait(&dempty[pr], pp ^ 1u);
                 if ((!f_ok && !mbar_wait_bounded(&full[slot], ph, a.budget, a.status)) ||
-                    (!c_ok && !mbar_wait_bounded(&conv[aslot], aph, a.budget, a.status))) { misc[1] = 1; break; }
+                    (!c_ok && !mbar_wait_bounded(&conv[slot], ph, a.budget, a.status)) ||
+                    (!d_ok && !mbar_wait_bounded(&dempty[pr], pp ^ 1u, a.budget, a.status))) {
+                    misc[1] = 1;
+                    break;
+                }
                 tc_fence_after();
-                bool ok = true;
-                for (int j = 0; j < BPS; ++j) {
-                    const int b = BPS * s + j;
-                    if (b >= nb) break;
-                    if (!mbar_test_wait(&dempty[buf], dpar) && !mbar_wait_bounded(&dempty[buf], dpar, a.budget, a.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                const uint32_t abase = sbase + OFF_A + slot * TILE;
+                const uint32_t bbase = sbase + OFF_ACT + slot * TILE;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (2 * s + j >= nb) break;
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t acol = tmem + A_COL0 + aslot * A_COLS + j * 16 + kk * 8;
-                        const uint64_t bdesc = smem_desc_sw128(sbase + OFF_ACT + slot * ACT_BYTES + (j >> 1) * ACT_SUB +
-                                                               (j & 1) * 64 + kk * 32);
-                        tc_mma_ts(tmem + buf * BN, acol, bdesc, kIdesc, (uint32_t)kk);
+                        const uint32_t off = (uint32_t)(j * 64 + kk * 32);
+                        tc_mma_ss(tmem + (uint32_t)((2 * pr + j) * BN), smem_desc_sw128(abase + off),
+                                  smem_desc_sw128(bbase + off), kIdesc, (uint32_t)kk);
                     }
-                    tc_commit(smem_u32(&dfull[buf]));
-                    if (++buf == ND) { buf = 0; dpar ^= 1u; }
                 }
+                tc_commit(smem_u32(&dfull[pr]));
                 tc_commit(smem_u32(&empty[slot]));
-                tc_commit(smem_u32(&aempty[aslot]));
-                if (!ok) { misc[1] = 1; break; }
             }
             // every MMA issued so far has completed once this barrier flips
             tc_commit(smem_u32(finalb));
             mbar_wait_bounded(finalb, 0, a.budget, nullptr);
         }
     } else if (warp >= CONV_WARP0 && warp < CONV_WARP0 + 4) {
-        // ------------------------------------------------------------ int4 -> fp16 into TMEM
-        const int q = warp & 3;
-        const int r = q * 32 + lane;
+        // ------------------------------------------------------------ int4 -> fp16 into shared memory
+        // Thread r writes its row's 64 fp16 weights of the stage as 8 chunks of
+        // 16 bytes, chunk c at position c ^ (r % 8) of the row's 128 bytes: the
+        // 128-byte swizzled K-major layout the MMA descriptor reads.
+        const int r = (warp - CONV_WARP0) * 32 + lane;
         for (int s = 0; s < nst; ++s) {
-            const int slot = s % S_SM, aslot = s % S_A;
-            const uint32_t ph = (uint32_t)(s / S_SM) & 1u, aph = (uint32_t)(s / S_A) & 1u;
-            const bool f_ok = mbar_test_wait(&full[slot], ph);
-            const bool e_ok = mbar_test_wait(&aempty[aslot], aph ^ 1u);
-            if (!__all_sync(0xffffffffu, f_ok) && !warp_wait(&full[slot], ph, a, &misc[1])) break;
-            if (!__all_sync(0xffffffffu, e_ok) && !warp_wait(&aempty[aslot], aph ^ 1u, a, &misc[1])) break;
-            tc_fence_after();
+            const int slot = s % S_SM;
+            const uint32_t ph = (uint32_t)(s / S_SM) & 1u;
+            if (!warp_wait(&full[slot], ph, a, &misc[1])) break;
             const uint4 *src = reinterpret_cast<const uint4 *>(smem + OFF_W + slot * W_BYTES + r * (KS / 2));
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + A_COL0 + aslot * A_COLS;
+            const uint4 p0 = src[0], p1 = src[1];
+            const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            uint8_t *row = smem + OFF_A + slot * TILE + r * 128;
 #pragma unroll
-            for (int hh = 0; hh < KS / 64; ++hh) {
-                const uint4 p0 = src[2 * hh], p1 = src[2 * hh + 1];
-                const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-                uint32_t h[32];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) h[4 * j + i] = nibbles_to_half2(wd[j] >> (4 * i));
-                TC_ST32(taddr + hh * 32, h);
+            for (int c = 0; c < 8; ++c) {
+                uint4 v;
+                v.x = nibbles_to_half2(wd[c]);
+                v.y = nibbles_to_half2(wd[c] >> 4);
+                v.z = nibbles_to_half2(wd[c] >> 8);
+                v.w = nibbles_to_half2(wd[c] >> 12);
+                *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = v;
             }
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            tc_fence_before();
+            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&conv[aslot]);
+            if (lane == 0) mbar_arrive(&conv[slot]);
         }
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue
-        // Per block: two TMEM loads of 32 token columns each (this warp owns
-        // 64), 64 fp32 scale-multiply-adds per thread, release of the
-        // accumulator after the second load.  Ring positions advance by
-        // counters, not divisions.
+        // Per pair of blocks: one wait, four TMEM loads of 32 token columns
+        // (this warp owns 64), 128 fp32 scale-multiply-adds per thread, one
+        // release of the pair.
         const int e = warp - EPI_WARP0;
         const int q = warp & 3;                        // TMEM lane quarter this warp may access
         const int c0 = (e >> 2) * 64;                  // this warp's 64 token columns
@@ -328,70 +309,69 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
         const int n = n0 + r;
         const bool nok = n < a.N;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
-        const bool vec_sw = (nb % SXG) == 0;           // rows of s_w start 16-byte aligned
         const uint16_t *swrow = a.sw + (size_t)(nok ? n : 0) * nb;
         float acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-        auto load_sw = [&](int g, uint4 &v) {
-            if (!nok || g * SXG >= nb) { v = make_uint4(0u, 0u, 0u, 0u); return; }
-            if (vec_sw) { v = __ldg(reinterpret_cast<const uint4 *>(swrow + g * SXG)); return; }
-            auto one = [&](int i) -> uint32_t {
-                const int k = g * SXG + i;
-                return k < nb ? (uint32_t)__ldg(swrow + k) : 0u;
-            };
-            v = make_uint4(one(0) | (one(1) << 16), one(2) | (one(3) << 16), one(4) | (one(5) << 16), one(6) | (one(7) << 16));
-        };
-        uint4 swv = make_uint4(0u, 0u, 0u, 0u), swv_next;
-        load_sw(0, swv_next);
-        int buf = 0, g = 0, gi = 0, sxslot = 0;
-        uint32_t dpar = 0u, sxpar = 0u;
-        for (int b = 0; b < nb; ++b) {
-            if (gi == 0) {
-                swv = swv_next;
-                load_sw(g + 1, swv_next);
-                if (!mbar_test_wait(&sxfull[sxslot], sxpar) && !warp_wait(&sxfull[sxslot], sxpar, a, &misc[1])) break;
-            }
-            const uint32_t sw_pair = gi < 2 ? swv.x : gi < 4 ? swv.y : gi < 6 ? swv.z : swv.w;
-            const float swf = __half2float(__ushort_as_half((unsigned short)((gi & 1) ? (sw_pair >> 16) : (sw_pair & 0xffffu))));
-            if (!mbar_test_wait(&dfull[buf], dpar) && !warp_wait(&dfull[buf], dpar, a, &misc[1])) break;
-            tc_fence_after();
-            const float *sxp = reinterpret_cast<const float *>(smem + OFF_SX + sxslot * SX_BYTES) + gi * BN + c0;
+        // s_w of the next pair of blocks is loaded one pair ahead and kept as
+        // raw fp16 bits: converting right after the load would stall the warp
+        // on the global-load latency at every block.
+        unsigned short swn0 = nok ? __ldg(swrow) : (unsigned short)0;
+        unsigned short swn1 = (nok && nb > 1) ? __ldg(swrow + 1) : (unsigned short)0;
+        int sxslot = 0, gi = 0;
+        uint32_t sxpar = 0u;
+        for (int s = 0; s < nst; ++s) {
+            const int pr = s % NP;
+            const uint32_t pp = (uint32_t)(s / NP) & 1u;
+            if (!(mbar_test_wait(&dfull[pr], pp) || warp_wait(&dfull[pr], pp, a, &misc[1]))) break;
+            bool aborted = false;
+            const unsigned short swc0 = swn0, swc1 = swn1;
+            if (nok && 2 * s + 2 < nb) swn0 = __ldg(swrow + 2 * s + 2);
+            if (nok && 2 * s + 3 < nb) swn1 = __ldg(swrow + 2 * s + 3);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t d[32];
-                TC_LD32(tbase + (uint32_t)(buf * BN + h * 32), d);
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (h == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&dempty[buf]);
+            for (int j = 0; j < 2; ++j) {
+                const int b = 2 * s + j;
+                if (b >= nb) break;
+                const float swf = __half2float(__ushort_as_half(j ? swc1 : swc0));
+                if (gi == 0 && !(mbar_test_wait(&sxfull[sxslot], sxpar) || warp_wait(&sxfull[sxslot], sxpar, a, &misc[1]))) {
+                    aborted = true;
+                    break;
                 }
+                tc_fence_after();
+                const float *sxp = reinterpret_cast<const float *>(smem + OFF_SX + sxslot * SX_BYTES) + gi * BN + c0;
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 sx4 = *reinterpret_cast<const float4 *>(sxp + h * 32 + i);
-                    const float sxv[4] = {sx4.x, sx4.y, sx4.z, sx4.w};
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t d[32];
+                    TC_LD32(tbase + (uint32_t)((2 * pr + j) * BN + h * 32), d);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float dv = __uint_as_float(d[i + u]);
-                        acc[h * 32 + i + u] = fmaf(dv, swf * sxv[u], acc[h * 32 + i + u]);
-                        if (DEBUG) {
-                            const int m = m0 + c0 + h * 32 + i + u;
-                            if (nok && m < a.M) a.dots[((size_t)m * a.N + n) * nb + b] = (int32_t)dv;
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 sx4 = *reinterpret_cast<const float4 *>(sxp + h * 32 + i);
+                        const float sxv[4] = {sx4.x, sx4.y, sx4.z, sx4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float dv = __uint_as_float(d[i + u]);
+                            acc[h * 32 + i + u] = fmaf(dv, swf * sxv[u], acc[h * 32 + i + u]);
+                            if (DEBUG) {
+                                const int m = m0 + c0 + h * 32 + i + u;
+                                if (nok && m < a.M) a.dots[((size_t)m * a.N + n) * nb + b] = (int32_t)dv;
+                            }
                         }
                     }
                 }
+                if (gi == SXG - 1 || b == nb - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sxempty[sxslot]);
+                }
+                if (++gi == SXG) {
+                    gi = 0;
+                    if (++sxslot == S_SX) { sxslot = 0; sxpar ^= 1u; }
+                }
             }
-            if (gi == SXG - 1 || b == nb - 1) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sxempty[sxslot]);
-            }
-            if (++buf == ND) { buf = 0; dpar ^= 1u; }
-            if (++gi == SXG) {
-                gi = 0;
-                ++g;
-                if (++sxslot == S_SX) { sxslot = 0; sxpar ^= 1u; }
-            }
+            if (aborted) break;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dempty[pr]);
         }
         if (nok && misc[1] == 0u) {
 #pragma unroll
