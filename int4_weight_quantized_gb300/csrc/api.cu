@@ -147,8 +147,10 @@ static w4a8_status run_linear(const uint16_t *x, const void *packed_w, const uin
     if (path == W4A8_PATH_AUTO) path = w4a8_select_path(M, N, K);
     cudaGetLastError();
     if (path == W4A8_PATH_DECODE) {
-        if (gemv_stream_supported(M, N, K)) return launch_gemv_stream(x, packed_w, scales, M, N, K, out, dots, stream);
-        if (!gemv_supported(M < 8 ? M : 8, N, K)) return W4A8_ERR_UNSUPPORTED;
+        const bool v1 = gemv_supported(M < 8 ? M : 8, N, K);
+        if (gemv_stream_supported(M, N, K) && (!v1 || gemv_stream_preferred(M, N, K)))
+            return launch_gemv_stream(x, packed_w, scales, M, N, K, out, dots, stream);
+        if (!v1) return W4A8_ERR_UNSUPPORTED;
         return launch_gemv(x, packed_w, scales, M, N, K, out, dots, stream);
     }
     if (path == W4A8_PATH_PREFILL) {

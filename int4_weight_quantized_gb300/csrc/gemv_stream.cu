@@ -37,7 +37,9 @@ constexpr int CWARPS = 8;                   // consumer warps
 constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
 constexpr int STAGES = 8;
 constexpr int STAGE_TARGET = 32768;         // weight bytes per chunk (about)
-constexpr int MAX_SMEM = 110 * 1024;        // leaves room for a second CTA (next launch) per SM
+constexpr int SMEM_COTENANT = 110 * 1024;   // two CTAs per SM: the next launch's copies start early
+constexpr int SMEM_ALONE = 200 * 1024;      // one CTA per SM, for long rows or many tokens
+constexpr int RG_MAX = 4;                   // rows reduced together per warp (compile-time bound)
 
 struct StreamArgs {
     const uint16_t *x;
@@ -50,6 +52,7 @@ struct StreamArgs {
     int M, N, K, nb;
     int rows_per_cta;    // R
     int cr;              // rows per chunk
+    int rg;              // rows per warp and pass, <= RG_MAX and <= 8 / MT
     int sw_bulk;         // scales copied with the weights (nb % 8 == 0)
     size_t stage_bytes;  // weights + scales per stage, 16-byte multiple
     int nslots;          // ring slots (<= STAGES)
@@ -96,9 +99,13 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(CWARPS * 32) : "memory"); }
 
+// BPL > 0: K has BPL slices of 32 blocks and each lane keeps the activation
+// codes of its BPL blocks in registers.  BPL == 0: any K; the codes are read
+// from shared memory next to each weight block.
 template <int MT, int BPL, bool DEBUG>
 __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
-    constexpr int RG = MT <= 2 ? 4 : (MT <= 4 ? 2 : 1);    // rows reduced together per warp
+    constexpr int RG = (8 / MT) < RG_MAX ? (8 / MT) : RG_MAX;
+    const int rgr = a.rg;
     extern __shared__ __align__(16) uint8_t smem[];
     const Layout L = layout(MT, a.nb, a.stage_bytes, a.nslots);
     const int NS = a.nslots;
@@ -185,26 +192,29 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
     consumer_sync();
 
     // this lane's K blocks (lane + 32 j) and their activation codes, in registers
-    uint32_t qa[MT][BPL][8];
-    float sxr[MT][BPL];
-    int cbr[MT][BPL];
+    constexpr int BR = BPL > 0 ? BPL : 1;
+    uint32_t qa[MT][BR][8];
+    float sxr[MT][BR];
+    int cbr[MT][BR];
+    if constexpr (BPL > 0) {
 #pragma unroll
-    for (int j = 0; j < BPL; ++j) {
-        const int b = lane + 32 * j;
+        for (int j = 0; j < BPL; ++j) {
+            const int b = lane + 32 * j;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (b < a.nb) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(codes + ((size_t)m * a.nb + b) * 8);
-                const uint4 c0 = src[0], c1 = src[1];
-                qa[m][j][0] = c0.x; qa[m][j][1] = c0.y; qa[m][j][2] = c0.z; qa[m][j][3] = c0.w;
-                qa[m][j][4] = c1.x; qa[m][j][5] = c1.y; qa[m][j][6] = c1.z; qa[m][j][7] = c1.w;
-                sxr[m][j] = sxs[m * a.nb + b];
-                cbr[m][j] = cbs[m * a.nb + b];
-            } else {
+            for (int m = 0; m < MT; ++m) {
+                if (b < a.nb) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(codes + ((size_t)m * a.nb + b) * 8);
+                    const uint4 c0 = src[0], c1 = src[1];
+                    qa[m][j][0] = c0.x; qa[m][j][1] = c0.y; qa[m][j][2] = c0.z; qa[m][j][3] = c0.w;
+                    qa[m][j][4] = c1.x; qa[m][j][5] = c1.y; qa[m][j][6] = c1.z; qa[m][j][7] = c1.w;
+                    sxr[m][j] = sxs[m * a.nb + b];
+                    cbr[m][j] = cbs[m * a.nb + b];
+                } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) qa[m][j][i] = 0u;
-                sxr[m][j] = 0.0f;
-                cbr[m][j] = kMagicBits;
+                    for (int i = 0; i < 8; ++i) qa[m][j][i] = 0u;
+                    sxr[m][j] = 0.0f;
+                    cbr[m][j] = kMagicBits;
+                }
             }
         }
     }
@@ -221,42 +231,77 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
         const int rows = min(a.cr, nrows - c * a.cr);
         // RG consecutive rows per warp at a time: their shuffle reductions
         // are independent and overlap
-        for (int rb = warp * RG; rb < rows; rb += CWARPS * RG) {
+        for (int rb = warp * rgr; rb < rows; rb += CWARPS * rgr) {
             float v[RG][MT];
 #pragma unroll
             for (int g = 0; g < RG; ++g)
 #pragma unroll
                 for (int m = 0; m < MT; ++m) v[g][m] = 0.0f;
+            // one 32-block of row rr (weights at wp, scale swh) against every token
+            auto block = [&](int g, int n, int b, const uint8_t *wp, uint16_t swh, const uint32_t (*q)[8],
+                             const float *sxv, const int *cbv) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(wp);
+                const float swf = __half2float(__ushort_as_half(swh));
+                const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+                uint32_t lo[4], hi[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    lo[i] = nib_even(w4[i]);
+                    hi[i] = nib_odd(w4[i]);
+                }
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    int d = cbv[m];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        d = dp4a_us(lo[i], q[m][2 * i], d);
+                        d = dp4a_us(hi[i], q[m][2 * i + 1], d);
+                    }
+                    if (DEBUG && m < a.M) a.dots[((size_t)m * a.N + n) * a.nb + b] = d - kMagicBits;
+                    v[g][m] = fmaf(__int_as_float(d) - kMagic, swf * sxv[m], v[g][m]);
+                }
+            };
 #pragma unroll
             for (int g = 0; g < RG; ++g) {
                 const int rr = rb + g;
-                if (rr >= rows) break;
+                if (g >= rgr || rr >= rows) break;
                 const int n = r0 + c * a.cr + rr;
+                const uint8_t *wrow = wst + (size_t)rr * row_bytes;
+                if constexpr (BPL > 0) {
 #pragma unroll
-                for (int j = 0; j < BPL; ++j) {
-                    const int b = lane + 32 * j;
-                    if (b < a.nb) {
-                        const uint4 w = *reinterpret_cast<const uint4 *>(wst + (size_t)rr * row_bytes + (size_t)b * 16);
-                        const uint16_t swh = a.sw_bulk ? sst[(size_t)rr * a.nb + b] : __ldg(a.sw + (size_t)n * a.nb + b);
-                        const float swf = __half2float(__ushort_as_half(swh));
-                        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-                        uint32_t lo[4], hi[4];
+                    for (int j = 0; j < BPL; ++j) {
+                        const int b = lane + 32 * j;
+                        if (b < a.nb) {
+                            const uint16_t swh = a.sw_bulk ? sst[(size_t)rr * a.nb + b] : __ldg(a.sw + (size_t)n * a.nb + b);
+                            uint32_t q[MT][8];
+                            float sxv[MT];
+                            int cbv[MT];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            lo[i] = nib_even(w4[i]);
-                            hi[i] = nib_odd(w4[i]);
+                            for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) q[m][i] = qa[m][j][i];
+                                sxv[m] = sxr[m][j];
+                                cbv[m] = cbr[m][j];
+                            }
+                            block(g, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
                         }
+                    }
+                } else {
+                    for (int b = lane; b < a.nb; b += 32) {
+                        const uint16_t swh = a.sw_bulk ? sst[(size_t)rr * a.nb + b] : __ldg(a.sw + (size_t)n * a.nb + b);
+                        uint32_t q[MT][8];
+                        float sxv[MT];
+                        int cbv[MT];
 #pragma unroll
                         for (int m = 0; m < MT; ++m) {
-                            int d = cbr[m][j];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                d = dp4a_us(lo[i], qa[m][j][2 * i], d);
-                                d = dp4a_us(hi[i], qa[m][j][2 * i + 1], d);
-                            }
-                            if (DEBUG && m < a.M) a.dots[((size_t)m * a.N + n) * a.nb + b] = d - kMagicBits;
-                            v[g][m] = fmaf(__int_as_float(d) - kMagic, swf * sxr[m][j], v[g][m]);
+                            const uint4 *src = reinterpret_cast<const uint4 *>(codes + ((size_t)m * a.nb + b) * 8);
+                            const uint4 c0 = src[0], c1 = src[1];
+                            q[m][0] = c0.x; q[m][1] = c0.y; q[m][2] = c0.z; q[m][3] = c0.w;
+                            q[m][4] = c1.x; q[m][5] = c1.y; q[m][6] = c1.z; q[m][7] = c1.w;
+                            sxv[m] = sxs[m * a.nb + b];
+                            cbv[m] = cbs[m * a.nb + b];
                         }
+                        block(g, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
                     }
                 }
             }
@@ -274,7 +319,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
                 for (int m = 0; m < MT; ++m)
                     if (lane == g * MT + m) mine = v[g][m];
             const int g = lane / MT, m = lane - (lane / MT) * MT;
-            if (lane < RG * MT && rb + g < rows && m < a.M)
+            if (lane < rgr * MT && rb + g < rows && m < a.M)
                 a.out[(size_t)m * a.N + r0 + c * a.cr + rb + g] = __half_as_ushort(__float2half_rn(mine));
         }
         if (reuse) {
@@ -285,7 +330,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
 }
 
 struct Plan {
-    int MT, BPL, R, cr, sw_bulk, nslots;
+    int MT, BPL, R, cr, rg, sw_bulk, nslots;
     size_t stage_bytes, smem;
     int grid;
     bool ok;
@@ -293,35 +338,55 @@ struct Plan {
 
 constexpr int kSMs = 152;
 
+// Launch plan: each of (up to) 152 CTAs owns R consecutive rows, streamed in
+// chunks of cr rows through an nslots-deep ring.  Chunks aim at about a
+// quarter of the CTA's bytes (at least 32 KB).  When the ring does not fit,
+// fewer slots are tried before smaller chunks (down to two slots), first
+// within the co-resident budget, then with one CTA per SM; rows per warp and
+// pass (rg) shrink until a chunk keeps all eight consumer warps busy.
 Plan make_plan(int M, int N, int K) {
     Plan p{};
     const int nb = K / 32;
     p.MT = M < 8 ? M : 8;
     p.BPL = (nb + 31) / 32;
-    p.ok = (p.BPL == 1 || p.BPL == 2 || p.BPL == 4 || p.BPL == 8) && p.MT * p.BPL <= 8;
+    if (!((p.BPL == 1 || p.BPL == 2 || p.BPL == 4 || p.BPL == 8) && p.MT * p.BPL <= 8)) p.BPL = 0;
     const size_t row_bytes = (size_t)K / 2;
     p.sw_bulk = (nb % 8) == 0;
     p.R = (N + kSMs - 1) / kSMs;
     p.grid = (N + p.R - 1) / p.R;
-    // about four chunks per CTA, each a whole number of rows
     const size_t cta_bytes = (size_t)p.R * row_bytes;
     size_t target = (cta_bytes + 3) / 4;
     if (target < (size_t)STAGE_TARGET) target = STAGE_TARGET;
-    p.cr = (int)(target / row_bytes);
-    if (p.cr < 1) p.cr = 1;
-    if (p.cr > p.R) p.cr = p.R;
-    auto size_up = [&]() {
-        p.stage_bytes = ((size_t)p.cr * row_bytes + (p.sw_bulk ? (size_t)p.cr * nb * 2 : 0) + 15) & ~(size_t)15;
-        const int nch = (p.R + p.cr - 1) / p.cr;
+    int cr0 = (int)(target / row_bytes);
+    if (cr0 < 1) cr0 = 1;
+    if (cr0 > p.R) cr0 = p.R;
+    auto fit = [&](int cr, size_t limit) {
+        p.cr = cr;
+        p.stage_bytes = ((size_t)cr * row_bytes + (p.sw_bulk ? (size_t)cr * nb * 2 : 0) + 15) & ~(size_t)15;
+        const int nch = (p.R + cr - 1) / cr;
         p.nslots = nch < STAGES ? nch : STAGES;
-        p.smem = layout(p.MT, nb, p.stage_bytes, p.nslots).total;
+        for (;;) {
+            p.smem = layout(p.MT, nb, p.stage_bytes, p.nslots).total;
+            if (p.smem <= limit || p.nslots <= 2) break;
+            --p.nslots;
+        }
+        return p.smem <= limit;
     };
-    size_up();
-    while (p.smem > (size_t)MAX_SMEM && p.cr > 1) {      // shrink chunks until the ring fits
-        p.cr = (p.cr + 1) / 2;
-        size_up();
+    bool ok = false;
+    for (size_t limit : {(size_t)SMEM_COTENANT, (size_t)SMEM_ALONE}) {
+        for (int cr = cr0; cr >= 1 && !ok; cr = (cr == 1 ? 0 : (cr + 1) / 2)) {
+            ok = fit(cr, limit);
+            if (ok && cr < CWARPS && cr < cr0 && limit == SMEM_COTENANT) ok = false;   // try one CTA per SM first
+        }
+        if (ok) break;
     }
-    if (p.smem > (size_t)MAX_SMEM) p.ok = false;
+    if (!ok) {   // last resort: the smallest ring that fits alone
+        for (int cr = cr0; cr >= 1 && !ok; cr = (cr == 1 ? 0 : (cr + 1) / 2)) ok = fit(cr, SMEM_ALONE);
+    }
+    const int rg_cap = (8 / p.MT) < RG_MAX ? (8 / p.MT) : RG_MAX;
+    p.rg = rg_cap;
+    while (p.rg > 1 && p.cr < CWARPS * p.rg) p.rg /= 2;
+    p.ok = ok;
     return p;
 }
 
@@ -332,7 +397,7 @@ w4a8_status launch_t(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W4A8_ERR_CUDA;
     if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SMEM) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALONE) != cudaSuccess)
             return W4A8_ERR_CUDA;
         attr_done[dev] = 1;
     }
@@ -371,6 +436,14 @@ w4a8_status dispatch(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
         case 6 * 16 + 1: return launch_t<6, 1, DEBUG>(p, a, stream);
         case 7 * 16 + 1: return launch_t<7, 1, DEBUG>(p, a, stream);
         case 8 * 16 + 1: return launch_t<8, 1, DEBUG>(p, a, stream);
+        case 1 * 16 + 0: return launch_t<1, 0, DEBUG>(p, a, stream);
+        case 2 * 16 + 0: return launch_t<2, 0, DEBUG>(p, a, stream);
+        case 3 * 16 + 0: return launch_t<3, 0, DEBUG>(p, a, stream);
+        case 4 * 16 + 0: return launch_t<4, 0, DEBUG>(p, a, stream);
+        case 5 * 16 + 0: return launch_t<5, 0, DEBUG>(p, a, stream);
+        case 6 * 16 + 0: return launch_t<6, 0, DEBUG>(p, a, stream);
+        case 7 * 16 + 0: return launch_t<7, 0, DEBUG>(p, a, stream);
+        case 8 * 16 + 0: return launch_t<8, 0, DEBUG>(p, a, stream);
         default: return W4A8_ERR_UNSUPPORTED;
     }
 }
@@ -380,6 +453,11 @@ w4a8_status dispatch(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
 namespace w4a8_host {
 
 bool gemv_stream_supported(int M, int N, int K) { return make_plan(M < 8 ? M : 8, N, K).ok; }
+
+bool gemv_stream_preferred(int M, int N, int K) {
+    const Plan p = make_plan(M < 8 ? M : 8, N, K);
+    return p.ok && (p.BPL > 0 || p.MT <= 2);
+}
 
 w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const uint16_t *scales,
                                int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream) {
@@ -403,6 +481,7 @@ w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const ui
         a.nb = K / 32;
         a.rows_per_cta = p.R;
         a.cr = p.cr;
+        a.rg = p.rg;
         a.sw_bulk = p.sw_bulk;
         a.stage_bytes = p.stage_bytes;
         a.nslots = p.nslots;

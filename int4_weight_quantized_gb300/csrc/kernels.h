@@ -27,9 +27,13 @@ w4a8_status launch_gemv(const uint16_t *x, const void *packed_w, const uint16_t 
 bool gemv_supported(int M, int N, int K);
 
 // Decode GEMV that streams weight rows through a shared-memory ring with
-// bulk copies (programmatic dependent launch); supported when K/32 blocks
-// form 1, 2, 4 or 8 slices of 32 and the shared-memory plan fits.
+// bulk copies (programmatic dependent launch); supported when its
+// shared-memory plan (ring + the quantised activations) fits one SM.
 bool gemv_stream_supported(int M, int N, int K);
+// The streaming kernel is the better decode kernel when each lane can keep
+// its activation codes in registers or there are at most two tokens;
+// otherwise the cluster split-K kernel (when it supports the shape) is faster.
+bool gemv_stream_preferred(int M, int N, int K);
 w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const uint16_t *scales,
                                int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream);
 

@@ -90,7 +90,12 @@ def test_quantizer_bit_exact(w4, M, K, scale, outliers):
 
 # ---------------------------------------------------------- block dots
 
-DOT_SHAPES = [(1, 1, 32), (1, 37, 96), (2, 100, 1024), (3, 64, 1056), (8, 129, 2048), (5, 257, 4096)]
+# decode kernels by shape: codes in registers (K/32 in 1, 2, 4 or 8 slices of
+# 32 blocks and tokens x slices <= 8), codes read from shared memory (one or two
+# tokens, any K; long rows make small chunks, and the longest need one CTA per
+# SM), and the cluster split-K kernel (3 to 8 tokens with long rows)
+DOT_SHAPES = [(1, 1, 32), (1, 37, 96), (2, 100, 1024), (3, 64, 1056), (8, 129, 2048), (5, 257, 4096),
+              (1, 300, 3072), (2, 77, 14336), (1, 40, 14336), (1, 700, 14336), (1, 1500, 4096)]
 
 
 @pytest.mark.parametrize("path", [1, 2])
