@@ -36,7 +36,8 @@ using namespace w4a8;
 constexpr int CWARPS = 8;                   // consumer warps
 constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
 constexpr int STAGES = 8;
-constexpr int STAGE_TARGET = 32768;         // weight bytes per chunk (about)
+constexpr int STAGE_TARGET = 65536;         // weight bytes per chunk (at least; fewer, larger chunks
+                                            // shorten the work after the dependency wait)
 constexpr int SMEM_COTENANT = 110 * 1024;   // two CTAs per SM: the next launch's copies start early
 constexpr int SMEM_ALONE = 200 * 1024;      // one CTA per SM, for long rows or many tokens
 constexpr int RG_MAX = 4;                   // rows reduced together per warp (compile-time bound)
@@ -340,7 +341,8 @@ constexpr int kSMs = 152;
 
 // Launch plan: each of (up to) 152 CTAs owns R consecutive rows, streamed in
 // chunks of cr rows through an nslots-deep ring.  Chunks aim at about a
-// quarter of the CTA's bytes (at least 32 KB).  When the ring does not fit,
+// quarter of the CTA's bytes (at least 64 KB, so a CTA of up to 64 KB is one
+// chunk).  When the ring does not fit,
 // fewer slots are tried before smaller chunks (down to two slots), first
 // within the co-resident budget, then with one CTA per SM; rows per warp and
 // pass (rg) shrink until a chunk keeps all eight consumer warps busy.
