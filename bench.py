@@ -43,7 +43,9 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only-secondary", action="store_true",
-                    help="time only the secondary (prefill) workload and print its record")
+                    help="time only the secondary workloads and print their records")
+    ap.add_argument("--secondary", default="prefill,layers,sweep",
+                    help="comma list of secondary workloads to run: prefill, layers, sweep")
     return ap.parse_args()
 
 
@@ -231,7 +233,7 @@ def main():
     if args.only_secondary:
         hbm, bf16, _, peak_src = peaks()
         stream = torch.cuda.Stream(device=dev)
-        print(json.dumps(run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src)), flush=True)
+        print(json.dumps(run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, args.secondary)), flush=True)
         return
     W = [w for w in wl.workloads() if w.name == HEADLINE][0]
     lin = W.linears[0]
@@ -312,7 +314,7 @@ def main():
 
     secondary = []
     if not args.no_secondary:
-        secondary = run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src)
+        secondary = run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, args.secondary)
 
     cpu = None
     if rank == 0:
@@ -335,10 +337,24 @@ def main():
         dist.destroy_process_group()
 
 
-def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src):
-    """Prefill GEMM (M=512) in TOPS, timed with CUDA events on its stream."""
+def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, which="prefill,layers,sweep"):
+    """Secondary workloads: prefill GEMM (M=512) in TOPS, the 26-layer decode
+    step and the shape sweep, each timed with CUDA events on its stream."""
     import torch
+    which = {s.strip() for s in which.split(",") if s.strip()}
     res = []
+    if "prefill" in which:
+        res.append(run_prefill(w4, wl, dev, stream, bf16, peak_src))
+    if "layers" in which:
+        res.append(run_decoder_layers(w4, wl, dev, stream, hbm, peak_src))
+    if "sweep" in which:
+        res.append(run_sweep(w4, wl, dev, stream, hbm, bf16, peak_src))
+    return res
+
+
+def run_prefill(w4, wl, dev, stream, bf16, peak_src):
+    """Prefill GEMM (M=512) in TOPS: a CUDA graph of 8 calls over 4 weight sets."""
+    import torch
     W = [w for w in wl.workloads() if w.name == "prefill_ffn_up_m512_k2048_n8192"][0]
     lin = W.linears[0]
     x, codes, scales = wl.make_linear_inputs(lin, W.seed, 0)
@@ -371,15 +387,12 @@ def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src):
         e1.synchronize()
     per_call = e0.elapsed_time(e1) * 1e-3 / (n * reps)
     tops = lin.ops / per_call / 1e12
-    res.append({"workload": W.name, "value": tops, "unit": "TOPS (2*M*N*K int8-equivalent)",
+    return {"workload": W.name, "value": tops, "unit": "TOPS (2*M*N*K int8-equivalent)",
                 "us_per_call": per_call * 1e6,
                 "roofline": {"bound": "tensor", "achieved": tops, "peak": bf16, "unit": "TFLOP/s",
                              "frac": tops / bf16, "peak_source": peak_src,
                              "note": "contraction runs on fp16 tensor cores (exact for int4 x int8 codes); "
-                                     "peak is the dense fp16/bf16 tensor rate"}})
-    res.append(run_decoder_layers(w4, wl, dev, stream, hbm, peak_src))
-    res.append(run_sweep(w4, wl, dev, stream, hbm, bf16, peak_src))
-    return res
+                                     "peak is the dense fp16/bf16 tensor rate"}}
 
 
 def run_sweep(w4, wl, dev, stream, hbm, bf16, peak_src, sets=5, reps=20):
