@@ -92,6 +92,15 @@ w4a8_status w4a8_pack(const int8_t *w_codes, int N, int K, void *packed_w,
  * W4A8_PATH_AUTO (0) for an invalid shape. */
 int w4a8_select_path(int M, int N, int K);
 
+/* Number of CTAs along K per 128 x 128 output tile that the prefill path
+ * uses for this shape: 1, 2, 4 or 8 (a thread-block cluster whose CTAs each
+ * take a contiguous range of 32-blocks; their fp32 partial tiles are summed
+ * in a fixed order through distributed shared memory, so results are
+ * deterministic).  Short sequences leave most SMs idle with one CTA per
+ * tile; this spreads K over more of them.  Returns 0 for an invalid shape.
+ * Informational: w4a8_linear and w4a8_linear_ex choose it themselves. */
+int w4a8_prefill_splits(int M, int N, int K);
+
 /* Device workspace in bytes that w4a8_linear_ex needs for this shape and
  * path (W4A8_PATH_AUTO resolves as w4a8_select_path); 0 when none.  The
  * prefill path keeps the quantised activations there. */

@@ -48,6 +48,8 @@ def lib():
         L.w4a8_pack.argtypes = [P, i, i, P, P]
         L.w4a8_select_path.argtypes = [i, i, i]
         L.w4a8_select_path.restype = i
+        L.w4a8_prefill_splits.argtypes = [i, i, i]
+        L.w4a8_prefill_splits.restype = i
         L.w4a8_workspace_bytes.argtypes = [i, i, i, i]
         L.w4a8_workspace_bytes.restype = sz
         L.w4a8_linear.argtypes = [P, P, P, i, i, i, P, P]
@@ -96,6 +98,11 @@ def packed_bytes(N, K):
 
 def select_path(M, N, K):
     return lib().w4a8_select_path(M, N, K)
+
+
+def prefill_splits(M, N, K):
+    """CTAs along K per output tile that the prefill path uses (1, 2, 4 or 8)."""
+    return lib().w4a8_prefill_splits(M, N, K)
 
 
 def workspace_bytes(M, N, K, path=PATH_AUTO):

@@ -126,6 +126,11 @@ int w4a8_select_path(int M, int N, int K) {
     return W4A8_PATH_PREFILL;
 }
 
+int w4a8_prefill_splits(int M, int N, int K) {
+    if (!shape_ok(M, N, K)) return 0;
+    return prefill_splits(M, N, K);
+}
+
 size_t w4a8_workspace_bytes(int M, int N, int K, int path) {
     if (!shape_ok(M, N, K)) return 0;
     if (path == W4A8_PATH_AUTO) path = w4a8_select_path(M, N, K);

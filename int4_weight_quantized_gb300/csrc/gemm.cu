@@ -81,6 +81,8 @@ struct GemmArgs {
     int *status;
     long long budget;
     int M, N, K, nb;
+    int splits;              // CTAs of a cluster along K (1, 2, 4 or 8); blockIdx.z is the split
+    int bps;                 // 32-blocks per split (even)
 };
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
@@ -152,6 +154,59 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
     return ok;
 }
 
+// All threads of all CTAs of the cluster; release/acquire orders the shared
+// memory writes before it with the reads after it, cluster-wide.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local_addr, uint32_t rank) {
+    uint32_t ra;
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+    return ra;
+}
+
+// fp32 load from distributed shared memory.  Volatile, so it stays after the
+// cluster barrier, but without a memory clobber; callers issue a batch of
+// these before using any of the results.
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// Sum of the S partial tiles for W/2 columns of one row, in split order.
+// Thread t of the 256 epilogue threads takes row t % 128 and half t / 128 of
+// this CTA's W = 128/S columns.
+template <int S>
+__device__ __forceinline__ void reduce_splits(uint32_t red, int z, int t, int n0, int m0, const GemmArgs &a, bool ok) {
+    constexpr int W = BN / S, C = W / 2;
+    const int r = t & (BM - 1);
+    const int c_beg = z * W + (t >> 7) * C;
+    const int n = n0 + r;
+    uint32_t base[S];
+#pragma unroll
+    for (int zz = 0; zz < S; ++zz) base[zz] = dsmem_addr(red + (uint32_t)((c_beg * BM + r) * 4), (uint32_t)zz);
+#pragma unroll
+    for (int j0 = 0; j0 < C; j0 += 8) {
+        float v[8][S];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int zz = 0; zz < S; ++zz) v[j][zz] = (j0 + j < C) ? ld_dsmem_f32(base[zz] + (uint32_t)((j0 + j) * BM * 4)) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j0 + j >= C) break;
+            float s = 0.0f;
+#pragma unroll
+            for (int zz = 0; zz < S; ++zz) s += v[j][zz];
+            const int m = m0 + c_beg + j0 + j;
+            if (ok && n < a.N && m < a.M) a.out[(size_t)m * a.N + n] = __half_as_ushort(__float2half_rn(s));
+        }
+    }
+}
+
 template <bool DEBUG>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
@@ -169,7 +224,11 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
     const int nb = a.nb;
-    const int nst = (nb + 1) / 2;               // stages = accumulator pairs
+    // This CTA's K range: blocks [b0, b0 + nbl) of the row (all of it when
+    // there is one split).
+    const int b0 = blockIdx.z * a.bps;
+    const int nbl = max(0, min(nb, b0 + a.bps) - b0);
+    const int nst = (nbl + 1) / 2;              // stages = accumulator pairs
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S_SM; ++s) {
@@ -209,7 +268,7 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
             uint64_t *fb = main ? full : sxfull;
             uint64_t *eb = main ? empty : sxempty;
             int issued = 0;
-            const int nloads = main ? nst : (nb + SXG - 1) / SXG;
+            const int nloads = main ? nst : (nbl + SXG - 1) / SXG;
             for (int s = 0; s < nloads; ++s) {
                 const int slot = s % S;
                 const uint32_t ph = (uint32_t)(s / S) & 1u;
@@ -219,11 +278,11 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
                 }
                 if (main) {
                     mbar_arrive_expect_tx(&fb[slot], TILE + W_BYTES);
-                    tma_load_2d(sbase + OFF_ACT + slot * TILE, &tm_act, s * KS, m0, smem_u32(&fb[slot]));
-                    tma_load_2d(sbase + OFF_W + slot * W_BYTES, &tm_w, s * (KS / 2), n0, smem_u32(&fb[slot]));
+                    tma_load_2d(sbase + OFF_ACT + slot * TILE, &tm_act, b0 * 32 + s * KS, m0, smem_u32(&fb[slot]));
+                    tma_load_2d(sbase + OFF_W + slot * W_BYTES, &tm_w, b0 * 16 + s * (KS / 2), n0, smem_u32(&fb[slot]));
                 } else {
                     mbar_arrive_expect_tx(&fb[slot], SX_BYTES);
-                    tma_load_2d(sbase + OFF_SX + slot * SX_BYTES, &tm_sx, m0, SXG * s, smem_u32(&fb[slot]));
+                    tma_load_2d(sbase + OFF_SX + slot * SX_BYTES, &tm_sx, m0, b0 + SXG * s, smem_u32(&fb[slot]));
                 }
                 issued = s + 1;
             }
@@ -255,7 +314,7 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
                 const uint32_t bbase = sbase + OFF_ACT + slot * TILE;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    if (2 * s + j >= nb) break;
+                    if (2 * s + j >= nbl) break;
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
                         const uint32_t off = (uint32_t)(j * 64 + kk * 32);
@@ -309,15 +368,15 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
         const int n = n0 + r;
         const bool nok = n < a.N;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
-        const uint16_t *swrow = a.sw + (size_t)(nok ? n : 0) * nb;
+        const uint16_t *swrow = a.sw + (size_t)(nok ? n : 0) * nb + b0;
         float acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
         // s_w of the next pair of blocks is loaded one pair ahead and kept as
         // raw fp16 bits: converting right after the load would stall the warp
         // on the global-load latency at every block.
-        unsigned short swn0 = nok ? __ldg(swrow) : (unsigned short)0;
-        unsigned short swn1 = (nok && nb > 1) ? __ldg(swrow + 1) : (unsigned short)0;
+        unsigned short swn0 = (nok && nbl > 0) ? __ldg(swrow) : (unsigned short)0;
+        unsigned short swn1 = (nok && nbl > 1) ? __ldg(swrow + 1) : (unsigned short)0;
         int sxslot = 0, gi = 0;
         uint32_t sxpar = 0u;
         for (int s = 0; s < nst; ++s) {
@@ -326,12 +385,12 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
             if (!(mbar_test_wait(&dfull[pr], pp) || warp_wait(&dfull[pr], pp, a, &misc[1]))) break;
             bool aborted = false;
             const unsigned short swc0 = swn0, swc1 = swn1;
-            if (nok && 2 * s + 2 < nb) swn0 = __ldg(swrow + 2 * s + 2);
-            if (nok && 2 * s + 3 < nb) swn1 = __ldg(swrow + 2 * s + 3);
+            if (nok && 2 * s + 2 < nbl) swn0 = __ldg(swrow + 2 * s + 2);
+            if (nok && 2 * s + 3 < nbl) swn1 = __ldg(swrow + 2 * s + 3);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int b = 2 * s + j;
-                if (b >= nb) break;
+                const int b = 2 * s + j;        // local block; b0 + b in the row
+                if (b >= nbl) break;
                 const float swf = __half2float(__ushort_as_half(j ? swc1 : swc0));
                 if (gi == 0 && !(mbar_test_wait(&sxfull[sxslot], sxpar) || warp_wait(&sxfull[sxslot], sxpar, a, &misc[1]))) {
                     aborted = true;
@@ -354,12 +413,12 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
                             acc[h * 32 + i + u] = fmaf(dv, swf * sxv[u], acc[h * 32 + i + u]);
                             if (DEBUG) {
                                 const int m = m0 + c0 + h * 32 + i + u;
-                                if (nok && m < a.M) a.dots[((size_t)m * a.N + n) * nb + b] = (int32_t)dv;
+                                if (nok && m < a.M) a.dots[((size_t)m * a.N + n) * nb + b0 + b] = (int32_t)dv;
                             }
                         }
                     }
                 }
-                if (gi == SXG - 1 || b == nb - 1) {
+                if (gi == SXG - 1 || b == nbl - 1) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sxempty[sxslot]);
                 }
@@ -373,13 +432,35 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
             __syncwarp();
             if (lane == 0) mbar_arrive(&dempty[pr]);
         }
-        if (nok && misc[1] == 0u) {
+        if (a.splits > 1) {
+            // partial tile of this K range -> shared memory, column-major
+            // (the operand ring is idle now: every MMA has completed)
+            float *red = reinterpret_cast<float *>(smem + OFF_ACT);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) red[(c0 + i) * BM + r] = acc[i];
+        } else if (nok && misc[1] == 0u) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
                 const int m = m0 + c0 + i;
                 if (m < a.M) a.out[(size_t)m * a.N + n] = __half_as_ushort(__float2half_rn(acc[i]));
             }
         }
+    }
+
+    if (a.splits > 1) {
+        // Split-K: the CTAs of the cluster hold the partial tiles of their K
+        // ranges; CTA z sums columns [z*W, (z+1)*W) of all of them through
+        // distributed shared memory, in split order (fixed, deterministic).
+        cluster_sync();
+        if (warp >= EPI_WARP0) {
+            const int t = threadIdx.x - EPI_WARP0 * 32;
+            const uint32_t red = sbase + OFF_ACT;
+            const bool ok = misc[1] == 0u;
+            if (a.splits == 2) reduce_splits<2>(red, blockIdx.z, t, n0, m0, a, ok);
+            else if (a.splits == 4) reduce_splits<4>(red, blockIdx.z, t, n0, m0, a, ok);
+            else reduce_splits<8>(red, blockIdx.z, t, n0, m0, a, ok);
+        }
+        cluster_sync();   // no CTA leaves while a peer may still read its tile
     }
 
     tc_fence_before();
@@ -422,6 +503,29 @@ bool make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void
 
 int m_pad(int M) { return (M + BN - 1) / BN * BN; }
 
+constexpr int kSMs = 152;
+
+// Split-K factor: the tile grid alone (N/128 x M_pad/128 CTAs) leaves most
+// SMs idle for short sequences.  Measured on GB300, a call costs about
+// 0.5 us per 32-block of a CTA plus ~8 us fixed (quantisation pass, pipeline
+// fill, reduction), so pick S in {1, 2, 4, 8} minimising
+// waves(tiles * S) * (blocks per split + 16); ties keep the smaller S.
+int pick_splits(int tiles, int nb) {
+    int best = 1;
+    long best_cost = -1;
+    for (int S = 1; S <= 8; S *= 2) {
+        if (S > 1 && nb < 2 * S) break;
+        const int bps = 2 * ((nb + 2 * S - 1) / (2 * S));
+        const long waves = ((long)tiles * S + kSMs - 1) / kSMs;
+        const long cost = waves * (bps + 16);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = S;
+        }
+    }
+    return best;
+}
+
 template <bool DEBUG>
 w4a8_status launch_t(const CUtensorMap &ta, const CUtensorMap &tw, const CUtensorMap &ts, const GemmArgs &a,
                      dim3 grid, cudaStream_t stream) {
@@ -434,13 +538,32 @@ w4a8_status launch_t(const CUtensorMap &ta, const CUtensorMap &tw, const CUtenso
             return W4A8_ERR_CUDA;
         attr_set[dev] = true;
     }
-    gemm_w4a8_tc_kernel<DEBUG><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tw, ts, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)a.splits;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.splits > 1 ? 1 : 0;   // one split: a plain launch
+    if (cudaLaunchKernelEx(&cfg, gemm_w4a8_tc_kernel<DEBUG>, ta, tw, ts, a) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A8_ERR_CUDA;
+    }
     return w4a8_host::launch_status();
 }
 
 }  // namespace
 
 namespace w4a8_host {
+
+int prefill_splits(int M, int N, int K) {
+    return pick_splits(((N + BM - 1) / BM) * (m_pad(M) / BN), K / 32);
+}
 
 size_t prefill_workspace_bytes(int M, int N, int K) {
     (void)N;
@@ -478,7 +601,9 @@ w4a8_status launch_prefill(const uint16_t *x, const void *packed_w, const uint16
     a.K = K;
     a.nb = nb;
     if (!a.status) return W4A8_ERR_CUDA;
-    dim3 grid((unsigned)((N + BM - 1) / BM), (unsigned)(mp / BN), 1);
+    a.splits = prefill_splits(M, N, K);
+    a.bps = 2 * ((nb + 2 * a.splits - 1) / (2 * a.splits));
+    dim3 grid((unsigned)((N + BM - 1) / BM), (unsigned)(mp / BN), (unsigned)a.splits);
     return dots ? launch_t<true>(ta, tw, ts, a, grid, stream) : launch_t<false>(ta, tw, ts, a, grid, stream);
 }
 

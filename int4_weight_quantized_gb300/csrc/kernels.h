@@ -39,6 +39,8 @@ w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const ui
 
 // Prefill path: quantisation pass into `workspace`, then the tensor-core GEMM.
 size_t prefill_workspace_bytes(int M, int N, int K);
+// CTAs along K per output tile of the prefill GEMM (1, 2, 4 or 8).
+int prefill_splits(int M, int N, int K);
 w4a8_status launch_prefill(const uint16_t *x, const void *packed_w, const uint16_t *scales,
                            int M, int N, int K, uint16_t *out, int32_t *dots, void *workspace,
                            cudaStream_t stream);

@@ -111,6 +111,27 @@ def test_block_dots_bit_exact(w4, path, M, N, K):
     assert_fp16_close(_np(y), oracle.linear(x.numpy(), codes.numpy(), scales.numpy()), f"y {M}x{N}x{K}")
 
 
+# shapes whose prefill tiles run as 1, 2, 4 and 8 CTAs along K (cluster
+# split-K with a fixed-order reduction in distributed shared memory)
+SPLIT_SHAPES = [((200, 10240, 256), 1), ((65, 8192, 512), 2), ((33, 2560, 1024), 4), ((16, 128, 1024), 8),
+                ((130, 70, 320), 4)]
+
+
+@pytest.mark.parametrize("shape,splits", SPLIT_SHAPES)
+def test_prefill_split_k_bit_exact(w4, shape, splits):
+    M, N, K = shape
+    assert w4.prefill_splits(M, N, K) == splits
+    x = wl.make_x(M, K, seed=500 + M, outlier_frac=0.01)
+    codes, scales = wl.make_weights(N, K, seed=600 + N, s_lo=-0.01, s_hi=0.01)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    dots, y = w4.debug_block_dots(xd, packed, sd, path=2)
+    q, _ = oracle.quantize_act(x.numpy())
+    assert np.array_equal(_np(dots), oracle.block_dots(q, codes.numpy()))
+    ref = oracle.linear(x.numpy(), codes.numpy(), scales.numpy())
+    assert_fp16_close(_np(y), ref, f"debug {M}x{N}x{K}")
+    assert_fp16_close(_np(w4.linear(xd, packed, sd, path=2)), ref, f"linear {M}x{N}x{K}")
+
+
 # ---------------------------------------------------------------- linear
 
 EDGE_SHAPES = ([(M, 67, 160) for M in range(1, 10)] + [(15, 33, 64), (16, 256, 512), (17, 50, 96),
