@@ -35,9 +35,10 @@ class Oracle:
         L.oracle_block_dots.argtypes = [P, P, i, i, i, P]
         L.oracle_linear.argtypes = [P, P, P, i, i, i, P, P]
         L.oracle_linear_f64.argtypes = [P, P, P, i, i, i, P]
+        L.oracle_linear_gated.argtypes = [P, P, P, i, i, i, i, P]
         L.oracle_unpack_weights.argtypes = [P, i, i, P]
         for f in ("oracle_quantize_act", "oracle_block_dots", "oracle_linear",
-                  "oracle_linear_f64", "oracle_unpack_weights"):
+                  "oracle_linear_f64", "oracle_linear_gated", "oracle_unpack_weights"):
             getattr(L, f).restype = ctypes.c_int
         self.L = L
         self.path = path
@@ -78,6 +79,18 @@ class Oracle:
         acc = np.empty((M, N), np.float32)
         _check(self.L.oracle_linear(_ptr(x), _ptr(w), _ptr(sw), M, N, K, _ptr(y), _ptr(acc)), "linear")
         return (y, acc) if return_acc else y
+
+    def linear_gated(self, x, w, sw, act):
+        """Gated pair: w int8 [2N][K] and sw fp16 [2N][K/32] stack gate over up rows;
+        act 1 = SiLU, 2 = GELU (tanh form) -> y fp16 [M][N] = act(gate) * up."""
+        x = np.ascontiguousarray(x, np.float16)
+        w = np.ascontiguousarray(w, np.int8)
+        sw = np.ascontiguousarray(sw, np.float16)
+        M, K = x.shape
+        N = w.shape[0] // 2
+        y = np.empty((M, N), np.float16)
+        _check(self.L.oracle_linear_gated(_ptr(x), _ptr(w), _ptr(sw), M, N, K, int(act), _ptr(y)), "linear_gated")
+        return y
 
     def linear_f64(self, x, w, sw):
         """fp64 dequantise-then-multiply of the same codes and scales -> float64 [M][N]."""
@@ -125,6 +138,10 @@ def linear(x, w, sw, return_acc=False):
 
 def linear_f64(x, w, sw):
     return get().linear_f64(x, w, sw)
+
+
+def linear_gated(x, w, sw, act):
+    return get().linear_gated(x, w, sw, act)
 
 
 def unpack_weights(packed, N, K):

@@ -168,6 +168,36 @@ int oracle_linear(const uint16_t *x, const int8_t *w, const uint16_t *sw,
     return rc;
 }
 
+/* ---- gated pair (gate rows over up rows), element-wise epilogue ---- */
+
+static double activation(int act, double g)
+{
+    if (act == 1) return g / (1.0 + exp(-g));
+    /* tanh form of GELU; sqrt(2/pi) written out from its definition */
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * g * (1.0 + tanh(c * (g + 0.044715 * g * g * g)));
+}
+
+int oracle_linear_gated(const uint16_t *x, const int8_t *w, const uint16_t *sw,
+                        int M, int N, int K, int act, uint16_t *y)
+{
+    if (M < 0 || N < 0 || K <= 0 || K % BLOCK != 0 || (act != 1 && act != 2)) return -1;
+    size_t cells = (size_t)M * (size_t)(2 * N);
+    uint16_t *y2 = (uint16_t *)malloc(sizeof(uint16_t) * (cells ? cells : 1));
+    float *acc = (float *)malloc(sizeof(float) * (cells ? cells : 1));
+    if (!y2 || !acc) { free(y2); free(acc); return -4; }
+    int rc = oracle_linear(x, w, sw, M, 2 * N, K, y2, acc);
+    for (int m = 0; m < M && rc == 0; ++m)
+        for (int n = 0; n < N; ++n) {
+            double g = (double)acc[(size_t)m * 2 * N + n];
+            double u = (double)acc[(size_t)m * 2 * N + N + n];
+            y[(size_t)m * N + n] = oracle_float_to_half((float)(activation(act, g) * u));
+        }
+    free(y2);
+    free(acc);
+    return rc;
+}
+
 int oracle_linear_f64(const uint16_t *x, const int8_t *w, const uint16_t *sw,
                       int M, int N, int K, double *ref)
 {

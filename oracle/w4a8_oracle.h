@@ -51,6 +51,18 @@ int oracle_block_dots(const int8_t *q, const int8_t *w, int M, int N, int K,
 int oracle_linear(const uint16_t *x, const int8_t *w, const uint16_t *sw,
                   int M, int N, int K, uint16_t *y, float *acc);
 
+/* Gated pair of linears ("Scaling On-Device GPU Inference for Large
+ * Generative Models", sciencestack.ai, Figure 4 left: element-wise operators
+ * of two branches fused with a fully connected operator).  w [2N][K] and
+ * sw [2N][K/32] stack the gate rows (0..N-1) over the up rows (N..2N-1);
+ * g and u are the fp32 sums oracle_linear computes for rows n and N+n, and
+ *   y[m][n] = fp16( act(g) * u ),   act evaluated and multiplied in fp64,
+ *   rounded to fp32, then to fp16 (both round to nearest even).
+ * act 1 = SiLU:            g / (1 + exp(-g))
+ * act 2 = GELU, tanh form: 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) */
+int oracle_linear_gated(const uint16_t *x, const int8_t *w, const uint16_t *sw,
+                        int M, int N, int K, int act, uint16_t *y);
+
 /* Checker: the same dequantised product in fp64,
  * ref[m][n] = sum_b sum_k (double)sw*w * (double)sx*q, with the codes and
  * activation scales of oracle_quantize_act. */

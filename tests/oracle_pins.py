@@ -286,4 +286,73 @@ def pin_unpack_layout(orc):
     assert np.all(w[1] == 0)
 
 
+def _gated_closed_form_case(act):
+    """x of 127*(m+1) everywhere (s_x = m+1 exactly, every code 127); gate row
+    n all codes cg[n] with block scales 2^-(10+n), up row n all codes cu[n]
+    with 2^-(8+n).  Every block dot is 32*127*code and every product is exact
+    in fp32, so g and u are known in closed form; act(g)*u follows from the
+    activation's definition with Python's math library."""
+    import math
+    M, N, K = 2, 3, 64
+    nb = K // 32
+    cg, cu = [-3, 2, 5], [7, -8, 1]
+    x = np.array([[127.0 * (m + 1)] * K for m in range(M)], np.float16)
+    w = np.zeros((2 * N, K), np.int8)
+    sw = np.zeros((2 * N, nb), np.float16)
+    for n in range(N):
+        w[n, :] = cg[n]
+        w[N + n, :] = cu[n]
+        sw[n, :] = 2.0 ** -(10 + n)
+        sw[N + n, :] = 2.0 ** -(8 + n)
+    y = np.zeros((M, N), np.float16)
+    for m in range(M):
+        for n in range(N):
+            g = nb * 32 * 127 * cg[n] * 2.0 ** -(10 + n) * (m + 1)
+            u = nb * 32 * 127 * cu[n] * 2.0 ** -(8 + n) * (m + 1)
+            if act == 1:
+                a = g / (1.0 + math.exp(-g))
+            else:
+                a = 0.5 * g * (1.0 + math.tanh(math.sqrt(2.0 / math.pi) * (g + 0.044715 * g ** 3)))
+            y[m, n] = np.float16(np.float32(a * u))
+    return x, w, sw, y
+
+
+def pin_gated_silu_closed_form(orc):
+    x, w, sw, y = _gated_closed_form_case(1)
+    assert np.array_equal(orc.linear_gated(x, w, sw, 1).view(np.uint16), y.view(np.uint16))
+
+
+def pin_gated_gelu_closed_form(orc):
+    x, w, sw, y = _gated_closed_form_case(2)
+    assert np.array_equal(orc.linear_gated(x, w, sw, 2).view(np.uint16), y.view(np.uint16))
+
+
+def pin_gated_special_values(orc):
+    """act(0) = 0 for both activations: zero gate rows give exact zeros; a
+    zero up row gives zeros; SiLU of a large gate is the gate itself, so with
+    unit up values y = g to fp16 precision."""
+    rng = _rng(31)
+    M, N, K = 3, 4, 96
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    w = rng.integers(-8, 8, (2 * N, K)).astype(np.int8)
+    sw = rng.uniform(0.001, 0.01, (2 * N, K // 32)).astype(np.float16)
+    for act in (1, 2):
+        wz = w.copy()
+        wz[:N] = 0
+        assert not np.any(orc.linear_gated(x, wz, sw, act).astype(np.float32))
+        wz = w.copy()
+        wz[N:] = 0
+        assert not np.any(orc.linear_gated(x, wz, sw, act).astype(np.float32))
+    # x = 127 (s_x = 1, codes 127); gate codes 7 with scale 1/2 over 3 blocks:
+    # g = 3*32*127*7/2 = 42672, and silu(g) = g in double precision; up codes 1
+    # with scale 2^-14 over 3 blocks: u = 3*4064*2^-14 = 0.744140625
+    xs = np.full((1, K), 127.0, np.float16)
+    wg = np.zeros((2, K), np.int8)
+    wg[0, :] = 7
+    wg[1, :] = 1
+    sg = np.array([[0.5] * 3, [2.0 ** -14] * 3], np.float16)
+    got = orc.linear_gated(xs, wg, sg, 1)
+    assert got[0, 0] == np.float16(np.float32(42672.0 * 0.744140625))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

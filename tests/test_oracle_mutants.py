@@ -40,6 +40,12 @@ MUTANTS = [
     ("unpack_no_offset", "(int8_t)((int)(byte & 0x0f) - 8)", "(int8_t)((int)(byte & 0x0f))"),
     ("unpack_nibbles_swapped", "w[(size_t)n * K + 2 * j] = (int8_t)((int)(byte & 0x0f) - 8);",
      "w[(size_t)n * K + 2 * j] = (int8_t)((int)(byte >> 4) - 8);"),
+    ("gated_branches_swapped", "double g = (double)acc[(size_t)m * 2 * N + n];",
+     "double g = (double)acc[(size_t)m * 2 * N + N + n];"),
+    ("silu_sign", "return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
+    ("gelu_cubic_coefficient", "(g + 0.044715 * g * g * g)", "(g + 0.044715 * g * g)"),
+    ("gated_up_row_offset", "double u = (double)acc[(size_t)m * 2 * N + N + n];",
+     "double u = (double)acc[(size_t)m * 2 * N + N + n - 1 + (n == 0)];"),
     ("f64_drops_weight_scale", "acc += (swd * (double)w[(size_t)n * K + k]) * (sxd * (double)q[k]);",
      "acc += ((double)w[(size_t)n * K + k]) * (sxd * (double)q[k]);"),
 ]
