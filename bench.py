@@ -45,7 +45,8 @@ def parse():
     ap.add_argument("--only-secondary", action="store_true",
                     help="time only the secondary workloads and print their records")
     ap.add_argument("--secondary", default="prefill,layers,sweep",
-                    help="comma list of secondary workloads to run: prefill, layers, sweep")
+                    help="comma list of secondary workloads to run: prefill, layers (both layer "
+                         "workloads), layers_fused, sweep")
     return ap.parse_args()
 
 
@@ -347,6 +348,8 @@ def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, which="prefill,layer
         res.append(run_prefill(w4, wl, dev, stream, bf16, peak_src))
     if "layers" in which:
         res.append(run_decoder_layers(w4, wl, dev, stream, hbm, peak_src))
+    if "layers_fused" in which or "layers" in which:
+        res.append(run_decoder_layers(w4, wl, dev, stream, hbm, peak_src, name="decoder_layers_m1_26x4_fused"))
     if "sweep" in which:
         res.append(run_sweep(w4, wl, dev, stream, hbm, bf16, peak_src))
     return res
@@ -441,26 +444,32 @@ def run_sweep(w4, wl, dev, stream, hbm, bf16, peak_src, sets=5, reps=20):
             "note": "decode rows are judged on GB/s against HBM, prefill rows on TOPS against the fp16 tensor peak"}
 
 
-def run_decoder_layers(w4, wl, dev, stream, hbm, peak_src, steps=20):
-    """One decode step over 26 decoder layers x 7 linears (M=1), captured as a
-    CUDA graph of 182 launches; effective HBM GB/s over the step."""
+def run_decoder_layers(w4, wl, dev, stream, hbm, peak_src, steps=20, name="decoder_layers_m1_26x7"):
+    """One decode step over 26 decoder layers (M=1), captured as a CUDA graph:
+    7 linears per layer (182 launches), or with name
+    decoder_layers_m1_26x4_fused the fused layer (qkv, o, gated gate/up,
+    down: 104 launches); effective HBM GB/s over the step."""
     import torch
-    W = [w for w in wl.workloads() if w.name == "decoder_layers_m1_26x7"][0]
+    W = [w for w in wl.workloads() if w.name == name][0]
     layers = W.extra["layers"]
     linears = []
     with torch.cuda.stream(stream):
         for layer in range(layers):
             for li, lin in enumerate(W.linears):
                 seed = W.seed + 100 * layer + li
-                c, s = wl.make_weights_on(dev, lin.N, lin.K, seed, lin.s_lo, lin.s_hi)
+                c, s = wl.make_weights_on(dev, lin.rows, lin.K, seed, lin.s_lo, lin.s_hi)
                 x = wl.make_x(lin.M, lin.K, seed, lin.outlier_frac).to(dev)
-                linears.append((x, w4.pack(c), s, torch.empty((lin.M, lin.N), dtype=torch.float16, device=dev)))
+                linears.append((x, w4.pack(c), s, torch.empty((lin.M, lin.N), dtype=torch.float16, device=dev),
+                                lin.gated))
                 del c
         step_bytes = layers * sum(l.bytes for l in W.linears)
 
         def step():
-            for x, p, s, o in linears:
-                w4.linear(x, p, s, out=o, path=w4.PATH_DECODE)
+            for x, p, s, o, act in linears:
+                if act:
+                    w4.linear_gated(x, p, s, act=act, out=o)
+                else:
+                    w4.linear(x, p, s, out=o, path=w4.PATH_DECODE)
         step()
         stream.synchronize()
         g = torch.cuda.CUDAGraph()

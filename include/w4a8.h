@@ -65,6 +65,12 @@ typedef enum {
     W4A8_PATH_PREFILL = 2   /* compute-bound tensor-core GEMM (tcgen05) after a quantisation pass */
 } w4a8_path;
 
+/* Activation of the gated pair's gate branch (w4a8_linear_gated). */
+typedef enum {
+    W4A8_ACT_SILU = 1,        /* g / (1 + exp(-g)) */
+    W4A8_ACT_GELU_TANH = 2    /* 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) */
+} w4a8_act;
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *w4a8_status_string(w4a8_status s);
 
@@ -126,6 +132,29 @@ w4a8_status w4a8_linear(const uint16_t *x, const void *packed_w, const uint16_t 
 w4a8_status w4a8_linear_ex(const uint16_t *x, const void *packed_w, const uint16_t *scales,
                            int M, int N, int K, uint16_t *out, int path,
                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Gated pair of linears: the element-wise operators of two branches fused
+ * with the fully connected operator ("Scaling On-Device GPU Inference for
+ * Large Generative Models", sciencestack.ai, Figure 4 left), as in a gated
+ * feed-forward block:
+ *   out[m][n] = act(g) * u,  g = W4A8 linear of x_m with gate row n,
+ *                            u = W4A8 linear of x_m with up row n,
+ * g and u in fp32 (each exactly the plain linear's sum before its fp16
+ * rounding on the fused route), act from w4a8_act, one fp16 rounding.
+ *   packed_gu  w4a8_packed_bytes(2N, K) bytes: w4a8_pack of a [2N][K] code
+ *              matrix whose rows 0..N-1 are the gate rows and N..2N-1 the up rows.
+ *   scales_gu  [2N][K/32] fp16, same row order.
+ *   out        [M][N] fp16.
+ * Decode shapes (see w4a8_gated_workspace_bytes == 0) run one fused kernel
+ * that streams each gate row with its up row and applies act(g)*u before the
+ * only store.  Other shapes run the linear over all 2N rows into `workspace`
+ * (then g and u are rounded to fp16 before the element-wise step) and an
+ * element-wise kernel.  Errors as w4a8_linear_ex; W4A8_ERR_INVALID_VALUE for
+ * an unknown act; W4A8_ERR_WORKSPACE when a needed workspace is missing. */
+size_t w4a8_gated_workspace_bytes(int M, int N, int K);
+w4a8_status w4a8_linear_gated(const uint16_t *x, const void *packed_gu, const uint16_t *scales_gu,
+                              int M, int N, int K, uint16_t *out, int act,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Debug: the activation quantiser alone, through the same device routine
  * the linear kernels use.  codes [M][K] int8 and sx [M][K/32] fp32, device. */

@@ -14,6 +14,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libw4a8.so")
 
+ACT_SILU = 1
+ACT_GELU_TANH = 2
+
 PATH_AUTO = 0
 PATH_DECODE = 1
 PATH_PREFILL = 2
@@ -50,6 +53,9 @@ def lib():
         L.w4a8_select_path.restype = i
         L.w4a8_prefill_splits.argtypes = [i, i, i]
         L.w4a8_prefill_splits.restype = i
+        L.w4a8_gated_workspace_bytes.argtypes = [i, i, i]
+        L.w4a8_gated_workspace_bytes.restype = sz
+        L.w4a8_linear_gated.argtypes = [P, P, P, i, i, i, P, i, P, sz, P]
         L.w4a8_workspace_bytes.argtypes = [i, i, i, i]
         L.w4a8_workspace_bytes.restype = sz
         L.w4a8_linear.argtypes = [P, P, P, i, i, i, P, P]
@@ -60,7 +66,7 @@ def lib():
         L.w4a8_get_device_status.argtypes = [P]
         L.w4a8_set_wait_budget.argtypes = [ctypes.c_longlong]
         L.w4a8_debug_wait_timeout.argtypes = [P]
-        for f in ("w4a8_pack", "w4a8_linear", "w4a8_linear_ex", "w4a8_linear_prefill_noalloc", "w4a8_debug_quantize_act",
+        for f in ("w4a8_pack", "w4a8_linear", "w4a8_linear_ex", "w4a8_linear_gated", "w4a8_linear_prefill_noalloc", "w4a8_debug_quantize_act",
                   "w4a8_debug_block_dots", "w4a8_get_device_status", "w4a8_set_wait_budget",
                   "w4a8_debug_wait_timeout"):
             getattr(L, f).restype = i
@@ -148,6 +154,33 @@ def linear(x, packed, scales, out=None, path=PATH_AUTO, workspace=None):
     wsb = workspace.numel() if workspace is not None else 0
     _check(lib().w4a8_linear_ex(_p(x), _p(packed), _p(scales), M, N, K, _p(out), path,
                                 _p(workspace), wsb, _stream()), "w4a8_linear_ex")
+    return out
+
+
+def gated_workspace_bytes(M, N, K):
+    return lib().w4a8_gated_workspace_bytes(M, N, K)
+
+
+def linear_gated(x, packed_gu, scales_gu, act=ACT_SILU, out=None, workspace=None):
+    """act(x . gate) * (x . up): packed_gu [2N, K/2] and scales_gu fp16 [2N, K/32]
+    stack the gate rows over the up rows; returns fp16 [M][N] (w4a8_linear_gated)."""
+    M, K = x.shape
+    N2 = scales_gu.shape[0]
+    if N2 % 2:
+        raise ValueError("scales_gu must have an even number of rows (gate rows over up rows)")
+    N = N2 // 2
+    _need(x, torch.float16, (M, K), "x")
+    _need(packed_gu, torch.uint8, (N2, K // 2), "packed_gu")
+    _need(scales_gu, torch.float16, (N2, K // 32), "scales_gu")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _need(out, torch.float16, (M, N), "out")
+    need = gated_workspace_bytes(M, N, K)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wsb = workspace.numel() if workspace is not None else 0
+    _check(lib().w4a8_linear_gated(_p(x), _p(packed_gu), _p(scales_gu), M, N, K, _p(out), int(act),
+                                   _p(workspace), wsb, _stream()), "w4a8_linear_gated")
     return out
 
 

@@ -196,6 +196,21 @@ w4a8_status w4a8_linear_ex(const uint16_t *x, const void *packed_w, const uint16
     return run_linear(x, packed_w, scales, M, N, K, out, nullptr, path, workspace, workspace_bytes, stream);
 }
 
+size_t w4a8_gated_workspace_bytes(int M, int N, int K) {
+    if (!shape_ok(M, N, K)) return 0;
+    return gated_workspace_bytes(M, N, K);
+}
+
+w4a8_status w4a8_linear_gated(const uint16_t *x, const void *packed_gu, const uint16_t *scales_gu,
+                              int M, int N, int K, uint16_t *out, int act,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    w4a8_status st = check_linear_args(x, packed_gu, scales_gu, M, N, K, out);
+    if (st != W4A8_OK) return st;
+    if (act != W4A8_ACT_SILU && act != W4A8_ACT_GELU_TANH) return W4A8_ERR_INVALID_VALUE;
+    cudaGetLastError();
+    return launch_gated(x, packed_gu, scales_gu, M, N, K, out, act, workspace, workspace_bytes, stream);
+}
+
 w4a8_status w4a8_debug_quantize_act(const uint16_t *x, int M, int K, int8_t *codes, float *sx,
                                     cudaStream_t stream) {
     if (!shape_ok(M, 1, K)) return W4A8_ERR_INVALID_VALUE;
@@ -250,3 +265,14 @@ w4a8_status w4a8_debug_wait_timeout(cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+namespace w4a8_host {
+
+size_t linear_workspace_bytes(int M, int N, int K) { return w4a8_workspace_bytes(M, N, K, W4A8_PATH_AUTO); }
+
+w4a8_status run_linear_auto(const uint16_t *x, const void *packed_w, const uint16_t *scales, int M, int N, int K,
+                            uint16_t *out, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return run_linear(x, packed_w, scales, M, N, K, out, nullptr, W4A8_PATH_AUTO, workspace, workspace_bytes, stream);
+}
+
+}  // namespace w4a8_host

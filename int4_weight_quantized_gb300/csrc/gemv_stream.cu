@@ -57,7 +57,16 @@ struct StreamArgs {
     int sw_bulk;         // scales copied with the weights (nb % 8 == 0)
     size_t stage_bytes;  // weights + scales per stage, 16-byte multiple
     int nslots;          // ring slots (<= STAGES)
+    int act;             // gated kernel: 1 = SiLU, 2 = GELU (tanh form)
 };
+
+// Activation of the gated kernel's gate branch, from its definition:
+// SiLU g / (1 + e^-g); GELU (tanh form) g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))).
+__device__ __forceinline__ float gate_act(int act, float g) {
+    if (act == 1) return g / (1.0f + expf(-g));
+    const float c = 0.7978845608028654f;    // sqrt(2/pi)
+    return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g)));
+}
 
 struct Layout {
     size_t ring, act_codes, act_sx, act_cb, part, bars, total;
@@ -103,8 +112,14 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 // BPL > 0: K has BPL slices of 32 blocks and each lane keeps the activation
 // codes of its BPL blocks in registers.  BPL == 0: any K; the codes are read
 // from shared memory next to each weight block.
-template <int MT, int BPL, bool DEBUG>
+// GATED: the weights stack N gate rows over N up rows; every chunk carries
+// the gate rows of the CTA's range and the matching up rows, and output row
+// n is act(gate_n . x) * (up_n . x) -- the element-wise operators of two
+// branches fused into the fully connected operator.
+template <int MT, int BPL, bool DEBUG, bool GATED>
 __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
+    static_assert(!(DEBUG && GATED), "the debug instantiation is the plain linear");
+    constexpr int NV = GATED ? 2 : 1;         // weight rows per output row
     constexpr int RG = (8 / MT) < RG_MAX ? (8 / MT) : RG_MAX;
     const int rgr = a.rg;
     extern __shared__ __align__(16) uint8_t smem[];
@@ -143,9 +158,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
                 const uint32_t wbytes = (uint32_t)(rows * row_bytes);
                 const uint32_t sbytes = a.sw_bulk ? (uint32_t)(rows * a.nb * 2) : 0u;
                 const uint32_t dst = smem_u32(smem + L.ring + (size_t)s * a.stage_bytes);
-                mbar_arrive_expect_tx(&full[s], wbytes + sbytes);
-                bulk_g2s(dst, a.pw + (size_t)rr * row_bytes, wbytes, smem_u32(&full[s]), pol);
-                if (sbytes) bulk_g2s(dst + (uint32_t)w_stage, a.sw + (size_t)rr * a.nb, sbytes, smem_u32(&full[s]), pol);
+                mbar_arrive_expect_tx(&full[s], NV * (wbytes + sbytes));
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    const size_t src_row = (size_t)rr + (size_t)v * a.N;     // up rows follow the N gate rows
+                    bulk_g2s(dst + (uint32_t)(v * w_stage), a.pw + src_row * row_bytes, wbytes, smem_u32(&full[s]), pol);
+                    if (sbytes)
+                        bulk_g2s(dst + (uint32_t)(NV * w_stage + (size_t)v * a.cr * a.nb * 2), a.sw + src_row * a.nb,
+                                 sbytes, smem_u32(&full[s]), pol);
+                }
                 if (c == NS - 1 || c == nchunks - 1) pdl_launch_dependents();
                 issued = c + 1;
             }
@@ -228,17 +249,17 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) return;
         const uint8_t *wst = smem + L.ring + (size_t)s * a.stage_bytes;
-        const uint16_t *sst = reinterpret_cast<const uint16_t *>(wst + w_stage);
+        const uint16_t *sst = reinterpret_cast<const uint16_t *>(wst + NV * w_stage);
         const int rows = min(a.cr, nrows - c * a.cr);
         // RG consecutive rows per warp at a time: their shuffle reductions
         // are independent and overlap
         for (int rb = warp * rgr; rb < rows; rb += CWARPS * rgr) {
-            float v[RG][MT];
+            float v[RG * NV][MT];      // [output row g][branch] flattened
 #pragma unroll
-            for (int g = 0; g < RG; ++g)
+            for (int g = 0; g < RG * NV; ++g)
 #pragma unroll
                 for (int m = 0; m < MT; ++m) v[g][m] = 0.0f;
-            // one 32-block of row rr (weights at wp, scale swh) against every token
+            // one 32-block of a weight row (weights at wp, scale swh) against every token
             auto block = [&](int g, int n, int b, const uint8_t *wp, uint16_t swh, const uint32_t (*q)[8],
                              const float *sxv, const int *cbv) {
                 const uint4 w = *reinterpret_cast<const uint4 *>(wp);
@@ -263,17 +284,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
                 }
             };
 #pragma unroll
-            for (int g = 0; g < RG; ++g) {
+            for (int gv = 0; gv < RG * NV; ++gv) {
+                const int g = gv / NV, br = gv % NV;   // output row, branch (0 gate / plain, 1 up)
                 const int rr = rb + g;
                 if (g >= rgr || rr >= rows) break;
                 const int n = r0 + c * a.cr + rr;
-                const uint8_t *wrow = wst + (size_t)rr * row_bytes;
+                const uint8_t *wrow = wst + (size_t)br * w_stage + (size_t)rr * row_bytes;
+                const uint16_t *srow = sst + (size_t)br * a.cr * a.nb + (size_t)rr * a.nb;
+                const uint16_t *sglob = a.sw + ((size_t)n + (size_t)br * a.N) * a.nb;
                 if constexpr (BPL > 0) {
 #pragma unroll
                     for (int j = 0; j < BPL; ++j) {
                         const int b = lane + 32 * j;
                         if (b < a.nb) {
-                            const uint16_t swh = a.sw_bulk ? sst[(size_t)rr * a.nb + b] : __ldg(a.sw + (size_t)n * a.nb + b);
+                            const uint16_t swh = a.sw_bulk ? srow[b] : __ldg(sglob + b);
                             uint32_t q[MT][8];
                             float sxv[MT];
                             int cbv[MT];
@@ -284,12 +308,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
                                 sxv[m] = sxr[m][j];
                                 cbv[m] = cbr[m][j];
                             }
-                            block(g, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
+                            block(gv, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
                         }
                     }
                 } else {
                     for (int b = lane; b < a.nb; b += 32) {
-                        const uint16_t swh = a.sw_bulk ? sst[(size_t)rr * a.nb + b] : __ldg(a.sw + (size_t)n * a.nb + b);
+                        const uint16_t swh = a.sw_bulk ? srow[b] : __ldg(sglob + b);
                         uint32_t q[MT][8];
                         float sxv[MT];
                         int cbv[MT];
@@ -302,14 +326,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
                             sxv[m] = sxs[m * a.nb + b];
                             cbv[m] = cbs[m * a.nb + b];
                         }
-                        block(g, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
+                        block(gv, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
                     }
                 }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-                for (int g = 0; g < RG; ++g)
+                for (int g = 0; g < RG * NV; ++g)
 #pragma unroll
                     for (int m = 0; m < MT; ++m) v[g][m] += __shfl_xor_sync(0xffffffffu, v[g][m], o);
             // lane g*MT + m stores row rb+g, token m
@@ -318,7 +342,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
             for (int g = 0; g < RG; ++g)
 #pragma unroll
                 for (int m = 0; m < MT; ++m)
-                    if (lane == g * MT + m) mine = v[g][m];
+                    if (lane == g * MT + m) mine = GATED ? gate_act(a.act, v[g * NV][m]) * v[g * NV + NV - 1][m] : v[g][m];
             const int g = lane / MT, m = lane - (lane / MT) * MT;
             if (lane < rgr * MT && rb + g < rows && m < a.M)
                 a.out[(size_t)m * a.N + r0 + c * a.cr + rb + g] = __half_as_ushort(__float2half_rn(mine));
@@ -346,13 +370,14 @@ constexpr int kSMs = 152;
 // fewer slots are tried before smaller chunks (down to two slots), first
 // within the co-resident budget, then with one CTA per SM; rows per warp and
 // pass (rg) shrink until a chunk keeps all eight consumer warps busy.
-Plan make_plan(int M, int N, int K) {
+Plan make_plan(int M, int N, int K, int nv = 1) {
+    // nv = weight rows per output row (2 for the gated kernel)
     Plan p{};
     const int nb = K / 32;
     p.MT = M < 8 ? M : 8;
     p.BPL = (nb + 31) / 32;
     if (!((p.BPL == 1 || p.BPL == 2 || p.BPL == 4 || p.BPL == 8) && p.MT * p.BPL <= 8)) p.BPL = 0;
-    const size_t row_bytes = (size_t)K / 2;
+    const size_t row_bytes = (size_t)nv * K / 2;
     p.sw_bulk = (nb % 8) == 0;
     p.R = (N + kSMs - 1) / kSMs;
     p.grid = (N + p.R - 1) / p.R;
@@ -364,7 +389,7 @@ Plan make_plan(int M, int N, int K) {
     if (cr0 > p.R) cr0 = p.R;
     auto fit = [&](int cr, size_t limit) {
         p.cr = cr;
-        p.stage_bytes = ((size_t)cr * row_bytes + (p.sw_bulk ? (size_t)cr * nb * 2 : 0) + 15) & ~(size_t)15;
+        p.stage_bytes = ((size_t)cr * row_bytes + (p.sw_bulk ? (size_t)nv * cr * nb * 2 : 0) + 15) & ~(size_t)15;
         const int nch = (p.R + cr - 1) / cr;
         p.nslots = nch < STAGES ? nch : STAGES;
         for (;;) {
@@ -392,9 +417,9 @@ Plan make_plan(int M, int N, int K) {
     return p;
 }
 
-template <int MT, int BPL, bool DEBUG>
+template <int MT, int BPL, bool DEBUG, bool GATED>
 w4a8_status launch_t(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
-    auto kern = gemv_stream_kernel<MT, BPL, DEBUG>;
+    auto kern = gemv_stream_kernel<MT, BPL, DEBUG, GATED>;
     static int attr_done[64] = {};   // per device: the opt-in shared-memory limit is set once
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W4A8_ERR_CUDA;
@@ -420,32 +445,32 @@ w4a8_status launch_t(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
     return w4a8_host::launch_status();
 }
 
-template <bool DEBUG>
+template <bool DEBUG, bool GATED>
 w4a8_status dispatch(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
     switch (p.MT * 16 + p.BPL) {
-        case 1 * 16 + 1: return launch_t<1, 1, DEBUG>(p, a, stream);
-        case 1 * 16 + 2: return launch_t<1, 2, DEBUG>(p, a, stream);
-        case 1 * 16 + 4: return launch_t<1, 4, DEBUG>(p, a, stream);
-        case 1 * 16 + 8: return launch_t<1, 8, DEBUG>(p, a, stream);
-        case 2 * 16 + 1: return launch_t<2, 1, DEBUG>(p, a, stream);
-        case 2 * 16 + 2: return launch_t<2, 2, DEBUG>(p, a, stream);
-        case 2 * 16 + 4: return launch_t<2, 4, DEBUG>(p, a, stream);
-        case 3 * 16 + 1: return launch_t<3, 1, DEBUG>(p, a, stream);
-        case 3 * 16 + 2: return launch_t<3, 2, DEBUG>(p, a, stream);
-        case 4 * 16 + 1: return launch_t<4, 1, DEBUG>(p, a, stream);
-        case 4 * 16 + 2: return launch_t<4, 2, DEBUG>(p, a, stream);
-        case 5 * 16 + 1: return launch_t<5, 1, DEBUG>(p, a, stream);
-        case 6 * 16 + 1: return launch_t<6, 1, DEBUG>(p, a, stream);
-        case 7 * 16 + 1: return launch_t<7, 1, DEBUG>(p, a, stream);
-        case 8 * 16 + 1: return launch_t<8, 1, DEBUG>(p, a, stream);
-        case 1 * 16 + 0: return launch_t<1, 0, DEBUG>(p, a, stream);
-        case 2 * 16 + 0: return launch_t<2, 0, DEBUG>(p, a, stream);
-        case 3 * 16 + 0: return launch_t<3, 0, DEBUG>(p, a, stream);
-        case 4 * 16 + 0: return launch_t<4, 0, DEBUG>(p, a, stream);
-        case 5 * 16 + 0: return launch_t<5, 0, DEBUG>(p, a, stream);
-        case 6 * 16 + 0: return launch_t<6, 0, DEBUG>(p, a, stream);
-        case 7 * 16 + 0: return launch_t<7, 0, DEBUG>(p, a, stream);
-        case 8 * 16 + 0: return launch_t<8, 0, DEBUG>(p, a, stream);
+        case 1 * 16 + 1: return launch_t<1, 1, DEBUG, GATED>(p, a, stream);
+        case 1 * 16 + 2: return launch_t<1, 2, DEBUG, GATED>(p, a, stream);
+        case 1 * 16 + 4: return launch_t<1, 4, DEBUG, GATED>(p, a, stream);
+        case 1 * 16 + 8: return launch_t<1, 8, DEBUG, GATED>(p, a, stream);
+        case 2 * 16 + 1: return launch_t<2, 1, DEBUG, GATED>(p, a, stream);
+        case 2 * 16 + 2: return launch_t<2, 2, DEBUG, GATED>(p, a, stream);
+        case 2 * 16 + 4: return launch_t<2, 4, DEBUG, GATED>(p, a, stream);
+        case 3 * 16 + 1: return launch_t<3, 1, DEBUG, GATED>(p, a, stream);
+        case 3 * 16 + 2: return launch_t<3, 2, DEBUG, GATED>(p, a, stream);
+        case 4 * 16 + 1: return launch_t<4, 1, DEBUG, GATED>(p, a, stream);
+        case 4 * 16 + 2: return launch_t<4, 2, DEBUG, GATED>(p, a, stream);
+        case 5 * 16 + 1: return launch_t<5, 1, DEBUG, GATED>(p, a, stream);
+        case 6 * 16 + 1: return launch_t<6, 1, DEBUG, GATED>(p, a, stream);
+        case 7 * 16 + 1: return launch_t<7, 1, DEBUG, GATED>(p, a, stream);
+        case 8 * 16 + 1: return launch_t<8, 1, DEBUG, GATED>(p, a, stream);
+        case 1 * 16 + 0: return launch_t<1, 0, DEBUG, GATED>(p, a, stream);
+        case 2 * 16 + 0: return launch_t<2, 0, DEBUG, GATED>(p, a, stream);
+        case 3 * 16 + 0: return launch_t<3, 0, DEBUG, GATED>(p, a, stream);
+        case 4 * 16 + 0: return launch_t<4, 0, DEBUG, GATED>(p, a, stream);
+        case 5 * 16 + 0: return launch_t<5, 0, DEBUG, GATED>(p, a, stream);
+        case 6 * 16 + 0: return launch_t<6, 0, DEBUG, GATED>(p, a, stream);
+        case 7 * 16 + 0: return launch_t<7, 0, DEBUG, GATED>(p, a, stream);
+        case 8 * 16 + 0: return launch_t<8, 0, DEBUG, GATED>(p, a, stream);
         default: return W4A8_ERR_UNSUPPORTED;
     }
 }
@@ -461,13 +486,16 @@ bool gemv_stream_preferred(int M, int N, int K) {
     return p.ok && (p.BPL > 0 || p.MT <= 2);
 }
 
-w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const uint16_t *scales,
-                               int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream) {
+namespace {
+
+w4a8_status run_stream(const uint16_t *x, const void *packed_w, const uint16_t *scales, int M, int N, int K,
+                       uint16_t *out, int32_t *dots, int act, cudaStream_t stream) {
     int *status = device_status_ptr();
     if (!status) return W4A8_ERR_CUDA;
+    const bool gated = act != 0;
     for (int m0 = 0; m0 < M; m0 += 8) {
         const int mc = (M - m0) < 8 ? (M - m0) : 8;
-        Plan p = make_plan(mc, N, K);
+        Plan p = make_plan(mc, N, K, gated ? 2 : 1);
         if (!p.ok) return W4A8_ERR_UNSUPPORTED;
         StreamArgs a;
         a.x = x + (size_t)m0 * K;
@@ -487,10 +515,32 @@ w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const ui
         a.sw_bulk = p.sw_bulk;
         a.stage_bytes = p.stage_bytes;
         a.nslots = p.nslots;
-        w4a8_status st = dots ? dispatch<true>(p, a, stream) : dispatch<false>(p, a, stream);
+        a.act = act;
+        w4a8_status st = gated ? dispatch<false, true>(p, a, stream)
+                               : (dots ? dispatch<true, false>(p, a, stream) : dispatch<false, false>(p, a, stream));
         if (st != W4A8_OK) return st;
     }
     return W4A8_OK;
+}
+
+}  // namespace
+
+w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const uint16_t *scales,
+                               int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream) {
+    return run_stream(x, packed_w, scales, M, N, K, out, dots, 0, stream);
+}
+
+bool gemv_stream_gated_supported(int M, int N, int K) { return make_plan(M < 8 ? M : 8, N, K, 2).ok; }
+
+bool gemv_stream_gated_preferred(int M, int N, int K) {
+    const Plan p = make_plan(M < 8 ? M : 8, N, K, 2);
+    return p.ok && (p.BPL > 0 || p.MT <= 2);
+}
+
+w4a8_status launch_gemv_stream_gated(const uint16_t *x, const void *packed_gu, const uint16_t *scales_gu,
+                                     int M, int N, int K, uint16_t *out, int act, cudaStream_t stream) {
+    if (act != 1 && act != 2) return W4A8_ERR_INVALID_VALUE;
+    return run_stream(x, packed_gu, scales_gu, M, N, K, out, nullptr, act, stream);
 }
 
 }  // namespace w4a8_host

@@ -34,6 +34,12 @@ bool gemv_stream_supported(int M, int N, int K);
 // its activation codes in registers or there are at most two tokens;
 // otherwise the cluster split-K kernel (when it supports the shape) is faster.
 bool gemv_stream_preferred(int M, int N, int K);
+// Gated pair (gate rows 0..N-1 over up rows N..2N-1 of one packed matrix):
+// out[m][n] = act(gate_n . x_m) * (up_n . x_m), act 1 = SiLU, 2 = GELU (tanh).
+bool gemv_stream_gated_supported(int M, int N, int K);
+bool gemv_stream_gated_preferred(int M, int N, int K);
+w4a8_status launch_gemv_stream_gated(const uint16_t *x, const void *packed_gu, const uint16_t *scales_gu,
+                                     int M, int N, int K, uint16_t *out, int act, cudaStream_t stream);
 w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const uint16_t *scales,
                                int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream);
 
@@ -41,6 +47,19 @@ w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const ui
 size_t prefill_workspace_bytes(int M, int N, int K);
 // CTAs along K per output tile of the prefill GEMM (1, 2, 4 or 8).
 int prefill_splits(int M, int N, int K);
+
+// The plain linear on the automatically chosen path (api.cu), and its
+// workspace size; used by the gated pair's unfused route.
+size_t linear_workspace_bytes(int M, int N, int K);
+w4a8_status run_linear_auto(const uint16_t *x, const void *packed_w, const uint16_t *scales, int M, int N, int K,
+                            uint16_t *out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+// Gated pair of linears (gated.cu): fused decode kernel when it takes the
+// shape, else the linear over 2N rows into the workspace + an element-wise pass.
+bool gated_fused(int M, int N, int K);
+size_t gated_workspace_bytes(int M, int N, int K);
+w4a8_status launch_gated(const uint16_t *x, const void *packed_gu, const uint16_t *scales_gu, int M, int N, int K,
+                         uint16_t *out, int act, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 w4a8_status launch_prefill(const uint16_t *x, const void *packed_w, const uint16_t *scales,
                            int M, int N, int K, uint16_t *out, int32_t *dots, void *workspace,
                            cudaStream_t stream);

@@ -66,11 +66,17 @@ class Linear:
     s_hi: float
     outlier_frac: float
     name: str = ""
+    gated: int = 0    # 0: plain linear; 1 SiLU / 2 GELU-tanh: gated pair with 2N weight rows
+
+    @property
+    def rows(self) -> int:
+        """Weight rows: N, or 2N (gate rows over up rows) for a gated pair."""
+        return 2 * self.N if self.gated else self.N
 
     @property
     def weight_bytes(self) -> int:
         """Algorithmic bytes of packed int4 weights plus fp16 block scales."""
-        return self.N * self.K // 2 + self.N * (self.K // BLOCK) * 2
+        return self.rows * self.K // 2 + self.rows * (self.K // BLOCK) * 2
 
     @property
     def bytes(self) -> int:
@@ -79,8 +85,8 @@ class Linear:
 
     @property
     def ops(self) -> int:
-        """Integer multiply-add operations of one call, counted as 2*M*N*K."""
-        return 2 * self.M * self.N * self.K
+        """Integer multiply-add operations of one call, counted as 2*M*rows*K."""
+        return 2 * self.M * self.rows * self.K
 
 
 @dataclass
@@ -97,9 +103,17 @@ class Workload:
 DECODER_LAYER = [("q", 2048, 2048), ("k", 256, 2048), ("v", 256, 2048), ("o", 2048, 2048),
                  ("gate", 8192, 2048), ("up", 8192, 2048), ("down", 2048, 8192)]
 
+# The same layer with the fusions of the pages' Figure 4 left ("Scaling
+# On-Device GPU Inference for Large Generative Models"): q, k and v as one
+# N=2560 projection of the shared input, and gate and up as one gated pair
+# (GELU, tanh form) whose element-wise product is the down projection's input.
+DECODER_LAYER_FUSED = [("qkv", 2560, 2048, 0), ("o", 2048, 2048, 0), ("gate_up", 8192, 2048, 2),
+                       ("down", 2048, 8192, 0)]
+
 
 def workloads():
-    """The five workloads, in order: tiny, decode FFN up, prefill FFN up, decoder layers, shape sweep."""
+    """The workloads, in order: tiny, decode FFN up, prefill FFN up, decoder layers, shape sweep,
+    fused decoder layers."""
     w = []
     w.append(Workload("tiny_m1_k256_n512", 0,
                       [Linear(1, 512, 256, 0.005, 0.02, 0.0, "tiny")],
@@ -121,11 +135,17 @@ def workloads():
             sweep.append(Linear(M, N, K, 0.001, 0.008, 0.01, f"sweep_m{M}_k{K}_n{N}"))
     w.append(Workload("shape_sweep", 4000, sweep,
                       description="K,N in {(4096,14336),(14336,4096)}, M in {1,4,8,64,512}"))
+    w.append(Workload("decoder_layers_m1_26x4_fused", 5000,
+                      [Linear(1, n, k, 0.002, 0.01, 0.01, nm, gated=act) for nm, n, k, act in DECODER_LAYER_FUSED],
+                      weight_sets=26,
+                      description="decode step over 26 decoder layers: qkv (N=2560), o, gated gate/up (GELU), down",
+                      extra={"layers": 26, "decode_steps": 128}))
     return w
 
 
 def make_linear_inputs(lin: Linear, seed: int, weight_set: int = 0):
-    """(x fp16 [M][K], codes int8 [N][K], scales fp16 [N][K/32]) for one linear of a workload."""
-    codes, scales = make_weights(lin.N, lin.K, seed + 1 + weight_set, lin.s_lo, lin.s_hi)
+    """(x fp16 [M][K], codes int8 [rows][K], scales fp16 [rows][K/32]) for one linear of a workload
+    (rows = N, or 2N with the gate rows over the up rows for a gated pair)."""
+    codes, scales = make_weights(lin.rows, lin.K, seed + 1 + weight_set, lin.s_lo, lin.s_hi)
     x = make_x(lin.M, lin.K, seed, lin.outlier_frac)
     return x, codes, scales

@@ -4,6 +4,8 @@ Integer work (packing, activation codes and scales, per-block dots) must be
 bit-exact; fp16 outputs must meet the tolerance of parity.py.  Inputs come
 from the seeded generators of int4_weight_quantized_gb300.workloads.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -132,6 +134,43 @@ def test_prefill_split_k_bit_exact(w4, shape, splits):
     assert_fp16_close(_np(w4.linear(xd, packed, sd, path=2)), ref, f"linear {M}x{N}x{K}")
 
 
+# --------------------------------------------------------- gated pair
+
+# decode shapes take the fused kernel (codes in registers, or codes from
+# shared memory with one or two tokens); the others take the linear over 2N
+# rows and the element-wise pass
+GATED_SHAPES = [(1, 64, 64, True), (1, 300, 2048, True), (2, 96, 3072, True), (3, 130, 1024, True),
+                (8, 200, 256, True), (1, 1000, 4096, True), (5, 70, 4096, False), (9, 70, 512, False),
+                (64, 128, 256, False), (200, 96, 320, False)]
+
+
+@pytest.mark.parametrize("act", [1, 2])
+@pytest.mark.parametrize("M,N,K,fused", GATED_SHAPES)
+def test_linear_gated(w4, M, N, K, fused, act):
+    assert (w4.gated_workspace_bytes(M, N, K) == 0) == fused
+    x = wl.make_x(M, K, seed=700 + M + K, outlier_frac=0.01)
+    codes, scales = wl.make_weights(2 * N, K, seed=800 + N + K, s_lo=0.002, s_hi=0.01)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    y = w4.linear_gated(xd, packed, sd, act=act)
+    ref = oracle.linear_gated(x.numpy(), codes.numpy(), scales.numpy(), act)
+    assert_fp16_close(_np(y), ref, f"gated act={act} {M}x{N}x{K}")
+
+
+def test_linear_gated_rejects_bad_act_and_missing_workspace(w4):
+    M, N, K = 16, 64, 256
+    x = wl.make_x(M, K, seed=3)
+    codes, scales = wl.make_weights(2 * N, K, seed=4, s_lo=0.002, s_hi=0.01)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    out = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    P = ctypes.c_void_p
+    st = w4.lib().w4a8_linear_gated(P(xd.data_ptr()), P(packed.data_ptr()), P(sd.data_ptr()), M, N, K,
+                                    P(out.data_ptr()), 3, P(0), 0, P(torch.cuda.current_stream().cuda_stream))
+    assert st == 1   # W4A8_ERR_INVALID_VALUE
+    st = w4.lib().w4a8_linear_gated(P(xd.data_ptr()), P(packed.data_ptr()), P(sd.data_ptr()), M, N, K,
+                                    P(out.data_ptr()), 1, P(0), 0, P(torch.cuda.current_stream().cuda_stream))
+    assert st == 7   # W4A8_ERR_WORKSPACE
+
+
 # ---------------------------------------------------------------- linear
 
 EDGE_SHAPES = ([(M, 67, 160) for M in range(1, 10)] + [(15, 33, 64), (16, 256, 512), (17, 50, 96),
@@ -207,11 +246,27 @@ def _sampled_check(w4, lin, seed, weight_set=0, n_cols=96, n_rows=48):
     return y
 
 
-@pytest.mark.parametrize("wi", range(5))
+def _sampled_check_gated(w4, lin, seed, n_cols=96):
+    """Full-size gated pair on the GPU; the oracle recomputes a sample of
+    output columns from their gate and up rows."""
+    x, codes, scales = wl.make_linear_inputs(lin, seed)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    y = _np(w4.linear_gated(xd, packed, sd, act=lin.gated))
+    g = np.random.default_rng(seed)
+    cols = np.unique(np.concatenate([[0, lin.N - 1], g.choice(lin.N, min(n_cols, lin.N), replace=False)]))
+    rows = np.concatenate([cols, lin.N + cols])
+    ref = oracle.linear_gated(x.numpy(), codes.numpy()[rows], scales.numpy()[rows], lin.gated)
+    assert_fp16_close(y[:, cols], ref, lin.name)
+
+
+@pytest.mark.parametrize("wi", range(len(wl.workloads())))
 def test_workloads_full_size(w4, wi):
     W = wl.workloads()[wi]
     for li, lin in enumerate(W.linears):
-        _sampled_check(w4, lin, W.seed + li * 100)
+        if lin.gated:
+            _sampled_check_gated(w4, lin, W.seed + li * 100)
+        else:
+            _sampled_check(w4, lin, W.seed + li * 100)
 
 
 def test_tiny_workload_exhaustive(w4):
