@@ -36,9 +36,10 @@ class Oracle:
         L.oracle_linear.argtypes = [P, P, P, i, i, i, P, P]
         L.oracle_linear_f64.argtypes = [P, P, P, i, i, i, P]
         L.oracle_linear_gated.argtypes = [P, P, P, i, i, i, i, P]
+        L.oracle_rmsnorm_quant.argtypes = [P, P, P, ctypes.c_float, i, i, P, P, P, P]
         L.oracle_unpack_weights.argtypes = [P, i, i, P]
         for f in ("oracle_quantize_act", "oracle_block_dots", "oracle_linear",
-                  "oracle_linear_f64", "oracle_linear_gated", "oracle_unpack_weights"):
+                  "oracle_linear_f64", "oracle_linear_gated", "oracle_rmsnorm_quant", "oracle_unpack_weights"):
             getattr(L, f).restype = ctypes.c_int
         self.L = L
         self.path = path
@@ -92,6 +93,24 @@ class Oracle:
         _check(self.L.oracle_linear_gated(_ptr(x), _ptr(w), _ptr(sw), M, N, K, int(act), _ptr(y)), "linear_gated")
         return y
 
+    def rmsnorm_quant(self, x, res, gamma, eps):
+        """x, res (or None) fp16 [M][K], gamma fp16 [K] -> (residual out fp16 [M][K],
+        normalised y fp16 [M][K], codes int8 [M][K], scales fp32 [M][K/32])."""
+        x = np.ascontiguousarray(x, np.float16)
+        M, K = x.shape
+        rp = None
+        if res is not None:
+            res = np.ascontiguousarray(res, np.float16)
+            rp = _ptr(res)
+        gamma = np.ascontiguousarray(gamma, np.float16)
+        ro = np.empty((M, K), np.float16)
+        y = np.empty((M, K), np.float16)
+        q = np.empty((M, K), np.int8)
+        sx = np.empty((M, K // 32), np.float32)
+        _check(self.L.oracle_rmsnorm_quant(_ptr(x), rp, _ptr(gamma), float(eps), M, K, _ptr(ro), _ptr(y), _ptr(q),
+                                           _ptr(sx)), "rmsnorm_quant")
+        return ro, y, q, sx
+
     def linear_f64(self, x, w, sw):
         """fp64 dequantise-then-multiply of the same codes and scales -> float64 [M][N]."""
         x = np.ascontiguousarray(x, np.float16)
@@ -142,6 +161,10 @@ def linear_f64(x, w, sw):
 
 def linear_gated(x, w, sw, act):
     return get().linear_gated(x, w, sw, act)
+
+
+def rmsnorm_quant(x, res, gamma, eps):
+    return get().rmsnorm_quant(x, res, gamma, eps)
 
 
 def unpack_weights(packed, N, K):

@@ -198,6 +198,40 @@ int oracle_linear_gated(const uint16_t *x, const int8_t *w, const uint16_t *sw,
     return rc;
 }
 
+/* ---- RMS normalisation (+ residual) emitting activation codes ---- */
+
+int oracle_rmsnorm_quant(const uint16_t *x, const uint16_t *res, const uint16_t *gamma, float eps,
+                         int M, int K, uint16_t *res_out, uint16_t *y, int8_t *q, float *sx)
+{
+    if (M < 0 || K <= 0 || K % BLOCK != 0 || !(eps >= 0.0f)) return -1;
+    uint16_t *yr = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)K);
+    float *r = (float *)malloc(sizeof(float) * (size_t)K);
+    if (!yr || !r) { free(yr); free(r); return -4; }
+    int rc = 0;
+    for (int m = 0; m < M && rc == 0; ++m) {
+        double ms = 0.0;
+        for (int k = 0; k < K; ++k) {
+            float h = oracle_half_to_float(x[(size_t)m * K + k]);
+            if (res) h = h + oracle_half_to_float(res[(size_t)m * K + k]);
+            uint16_t rb = oracle_float_to_half(h);
+            if (res_out) res_out[(size_t)m * K + k] = rb;
+            r[k] = oracle_half_to_float(rb);
+            ms += (double)r[k] * (double)r[k];
+        }
+        ms /= (double)K;
+        double inv = 1.0 / sqrt(ms + (double)eps);
+        for (int k = 0; k < K; ++k) {
+            double v = (double)r[k] * inv * (double)oracle_half_to_float(gamma[k]);
+            yr[k] = oracle_float_to_half((float)v);
+            if (y) y[(size_t)m * K + k] = yr[k];
+        }
+        rc = oracle_quantize_act(yr, 1, K, q + (size_t)m * K, sx + (size_t)m * (K / BLOCK));
+    }
+    free(yr);
+    free(r);
+    return rc;
+}
+
 int oracle_linear_f64(const uint16_t *x, const int8_t *w, const uint16_t *sw,
                       int M, int N, int K, double *ref)
 {

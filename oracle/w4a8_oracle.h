@@ -63,6 +63,20 @@ int oracle_linear(const uint16_t *x, const int8_t *w, const uint16_t *sw,
 int oracle_linear_gated(const uint16_t *x, const int8_t *w, const uint16_t *sw,
                         int M, int N, int K, int act, uint16_t *y);
 
+/* RMS normalisation with the residual add, emitting the linear's activation
+ * codes ("Scaling On-Device GPU Inference for Large Generative Models",
+ * sciencestack.ai, Figure 4 right: the residual connection and element-wise
+ * operations merged into the RMS normalisation operator; producer-side
+ * quantisation of the normalised activations).  Per token row m:
+ *   r[k]  = fp16( float(x[k]) + float(res[k]) )   (res may be NULL: r = x)
+ *   ms    = (1/K) sum_k r[k]^2                    (fp64)
+ *   y[k]  = fp16( float( r[k] / sqrt(ms + eps) * gamma[k] ) )   (fp64, then fp32, then fp16)
+ *   q, sx = oracle_quantize_act(y)
+ * res_out (may be NULL) receives r, the updated residual stream; y (may be
+ * NULL) the normalised fp16 row.  gamma [K] fp16; eps >= 0. */
+int oracle_rmsnorm_quant(const uint16_t *x, const uint16_t *res, const uint16_t *gamma, float eps,
+                         int M, int K, uint16_t *res_out, uint16_t *y, int8_t *q, float *sx);
+
 /* Checker: the same dequantised product in fp64,
  * ref[m][n] = sum_b sum_k (double)sw*w * (double)sx*q, with the codes and
  * activation scales of oracle_quantize_act. */

@@ -355,4 +355,59 @@ def pin_gated_special_values(orc):
     assert got[0, 0] == np.float16(np.float32(42672.0 * 0.744140625))
 
 
+def pin_rmsnorm_closed_form(orc):
+    """K=32, eps=0, unit gamma, no residual: a row of 16 threes and 16 fours has
+    mean square 12.5, so y = 3/sqrt(12.5) and 4/sqrt(12.5); a constant row c
+    gives y = sign(c) exactly, hence codes +-127 and scale 1/127."""
+    import math
+    K = 32
+    x = np.array([[3.0] * 16 + [4.0] * 16, [-5.0] * 32, [0.25] * 32], np.float16)
+    gamma = np.ones(K, np.float16)
+    ro, y, q, sx = orc.rmsnorm_quant(x, None, gamma, 0.0)
+    want0 = [np.float16(np.float32(3.0 / math.sqrt(12.5)))] * 16 + [np.float16(np.float32(4.0 / math.sqrt(12.5)))] * 16
+    assert np.array_equal(y[0].view(np.uint16), np.array(want0, np.float16).view(np.uint16))
+    assert np.all(y[1] == -1.0) and np.all(y[2] == 1.0)
+    assert np.all(q[1] == -127) and np.all(q[2] == 127)
+    assert sx[1, 0] == np.float32(1.0) / np.float32(127.0) and sx[2, 0] == sx[1, 0]
+    assert np.array_equal(ro.view(np.uint16), x.view(np.uint16))
+
+
+def pin_rmsnorm_residual_and_eps(orc):
+    """The residual stream is the fp16 sum x + res (IEEE addition in fp32, one
+    rounding); eps enters under the root: a zero row gives y = 0 with eps > 0,
+    and for a constant row c, y = c / sqrt(c^2 + eps)."""
+    import math
+    rng = _rng(41)
+    M, K = 3, 64
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    res = rng.standard_normal((M, K)).astype(np.float16)
+    gamma = np.ones(K, np.float16)
+    ro, _, _, _ = orc.rmsnorm_quant(x, res, gamma, 1e-6)
+    assert np.array_equal(ro.view(np.uint16), (x.astype(np.float32) + res.astype(np.float32)).astype(np.float16).view(np.uint16))
+    z = np.zeros((1, K), np.float16)
+    _, y, q, sx = orc.rmsnorm_quant(z, None, gamma, 1e-5)
+    assert not np.any(y.astype(np.float32)) and not np.any(q) and np.all(sx == 1.0)
+    c = np.full((1, K), 0.5, np.float16)
+    _, y, _, _ = orc.rmsnorm_quant(c, None, gamma, 0.25)
+    assert y[0, 0] == np.float16(np.float32(0.5 / math.sqrt(0.25 + 0.25)))
+
+
+def pin_rmsnorm_invariants(orc):
+    """With eps = 0 the norm is invariant to scaling the row by 2^j (codes and
+    scales identical); gamma * 2 doubles y exactly (same codes, scales * 2);
+    the codes are those of the activation quantiser applied to y."""
+    rng = _rng(43)
+    M, K = 4, 96
+    x = (rng.standard_normal((M, K)) * 3).astype(np.float16)
+    gamma = rng.uniform(0.5, 1.5, K).astype(np.float16)
+    _, y, q, sx = orc.rmsnorm_quant(x, None, gamma, 0.0)
+    _, y2, q2, sx2 = orc.rmsnorm_quant((x.astype(np.float32) * 4).astype(np.float16), None, gamma, 0.0)
+    assert np.array_equal(y.view(np.uint16), y2.view(np.uint16)) and np.array_equal(q, q2)
+    _, y3, q3, sx3 = orc.rmsnorm_quant(x, None, (gamma.astype(np.float32) * 2).astype(np.float16), 0.0)
+    assert np.array_equal(y3.astype(np.float32), y.astype(np.float32) * 2) and np.array_equal(q3, q)
+    assert np.array_equal(sx3, sx * 2)
+    qa, sa = orc.quantize_act(y)
+    assert np.array_equal(qa, q) and np.array_equal(sa, sx)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

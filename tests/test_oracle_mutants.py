@@ -46,6 +46,12 @@ MUTANTS = [
     ("gelu_cubic_coefficient", "(g + 0.044715 * g * g * g)", "(g + 0.044715 * g * g)"),
     ("gated_up_row_offset", "double u = (double)acc[(size_t)m * 2 * N + N + n];",
      "double u = (double)acc[(size_t)m * 2 * N + N + n - 1 + (n == 0)];"),
+    ("rmsnorm_sum_not_mean", "ms /= (double)K;", "ms /= 1.0;"),
+    ("rmsnorm_eps_outside_root", "double inv = 1.0 / sqrt(ms + (double)eps);", "double inv = 1.0 / (sqrt(ms) + (double)eps);"),
+    ("rmsnorm_no_gamma", "double v = (double)r[k] * inv * (double)oracle_half_to_float(gamma[k]);",
+     "double v = (double)r[k] * inv;"),
+    ("rmsnorm_residual_dropped", "if (res) h = h + oracle_half_to_float(res[(size_t)m * K + k]);", "(void)res;"),
+    ("rmsnorm_no_root", "double inv = 1.0 / sqrt(ms + (double)eps);", "double inv = 1.0 / (ms + (double)eps);"),
     ("f64_drops_weight_scale", "acc += (swd * (double)w[(size_t)n * K + k]) * (sxd * (double)q[k]);",
      "acc += ((double)w[(size_t)n * K + k]) * (sxd * (double)q[k]);"),
 ]
