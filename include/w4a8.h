@@ -156,6 +156,37 @@ w4a8_status w4a8_linear_gated(const uint16_t *x, const void *packed_gu, const ui
                               int M, int N, int K, uint16_t *out, int act,
                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* RMS normalisation with the residual add, quantising its output for the
+ * next linear (producer-side quantisation): the residual connection and the
+ * element-wise operations merged into the RMS normalisation operator
+ * ("Scaling On-Device GPU Inference for Large Generative Models",
+ * sciencestack.ai, Figure 4 right).  Per token row m:
+ *   r = fp16(x + residual)           (fp32 sum, one rounding; r = x when residual is NULL)
+ *   y = fp16(r / sqrt(mean_k(r^2) + eps) * gamma)   (fp32 arithmetic)
+ *   codes, sx = the activation quantiser applied to y (as in w4a8_debug_quantize_act)
+ *   x, residual      [M][K] fp16, device (residual may be NULL)
+ *   gamma            [K] fp16, device
+ *   residual_out     [M][K] fp16 or NULL: receives r (may alias neither input)
+ *   y_out            [M][K] fp16 or NULL: receives y
+ *   codes            [M][K] int8, natural k order; sx [M][K/32] fp32 -- the
+ *                    input of w4a8_linear_q8.
+ * eps must be finite and >= 0.  Asynchronous on `stream`. */
+w4a8_status w4a8_rmsnorm_quant(const uint16_t *x, const uint16_t *residual, const uint16_t *gamma, float eps,
+                               int M, int K, uint16_t *residual_out, uint16_t *y_out, int8_t *codes, float *sx,
+                               cudaStream_t stream);
+
+/* The linear on activations quantised by their producer: codes int8 [M][K]
+ * and sx fp32 [M][K/32] as w4a8_rmsnorm_quant writes them (codes in
+ * [-127, 127]; sx the block scales).  Same result as w4a8_linear of the fp16
+ * activations these codes came from.  Decode shapes run the streaming GEMV
+ * without its quantisation step; others convert the codes into the prefill
+ * layout in `workspace` (w4a8_linear_q8_workspace_bytes, 0 when none is
+ * needed) and run the tensor-core GEMM. */
+size_t w4a8_linear_q8_workspace_bytes(int M, int N, int K);
+w4a8_status w4a8_linear_q8(const int8_t *codes, const float *sx, const void *packed_w, const uint16_t *scales,
+                           int M, int N, int K, uint16_t *out, void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
 /* Debug: the activation quantiser alone, through the same device routine
  * the linear kernels use.  codes [M][K] int8 and sx [M][K/32] fp32, device. */
 w4a8_status w4a8_debug_quantize_act(const uint16_t *x, int M, int K, int8_t *codes,

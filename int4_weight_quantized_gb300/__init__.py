@@ -56,6 +56,10 @@ def lib():
         L.w4a8_gated_workspace_bytes.argtypes = [i, i, i]
         L.w4a8_gated_workspace_bytes.restype = sz
         L.w4a8_linear_gated.argtypes = [P, P, P, i, i, i, P, i, P, sz, P]
+        L.w4a8_rmsnorm_quant.argtypes = [P, P, P, ctypes.c_float, i, i, P, P, P, P, P]
+        L.w4a8_linear_q8_workspace_bytes.argtypes = [i, i, i]
+        L.w4a8_linear_q8_workspace_bytes.restype = sz
+        L.w4a8_linear_q8.argtypes = [P, P, P, P, i, i, i, P, P, sz, P]
         L.w4a8_workspace_bytes.argtypes = [i, i, i, i]
         L.w4a8_workspace_bytes.restype = sz
         L.w4a8_linear.argtypes = [P, P, P, i, i, i, P, P]
@@ -66,7 +70,8 @@ def lib():
         L.w4a8_get_device_status.argtypes = [P]
         L.w4a8_set_wait_budget.argtypes = [ctypes.c_longlong]
         L.w4a8_debug_wait_timeout.argtypes = [P]
-        for f in ("w4a8_pack", "w4a8_linear", "w4a8_linear_ex", "w4a8_linear_gated", "w4a8_linear_prefill_noalloc", "w4a8_debug_quantize_act",
+        for f in ("w4a8_pack", "w4a8_linear", "w4a8_linear_ex", "w4a8_linear_gated", "w4a8_rmsnorm_quant",
+                  "w4a8_linear_q8", "w4a8_linear_prefill_noalloc", "w4a8_debug_quantize_act",
                   "w4a8_debug_block_dots", "w4a8_get_device_status", "w4a8_set_wait_budget",
                   "w4a8_debug_wait_timeout"):
             getattr(L, f).restype = i
@@ -181,6 +186,47 @@ def linear_gated(x, packed_gu, scales_gu, act=ACT_SILU, out=None, workspace=None
     wsb = workspace.numel() if workspace is not None else 0
     _check(lib().w4a8_linear_gated(_p(x), _p(packed_gu), _p(scales_gu), M, N, K, _p(out), int(act),
                                    _p(workspace), wsb, _stream()), "w4a8_linear_gated")
+    return out
+
+
+def rmsnorm_quant(x, gamma, eps=1e-6, residual=None, residual_out=None, y_out=None, codes=None, sx=None):
+    """RMS norm (+ residual add) of x fp16 [M][K] with gamma fp16 [K], quantised for
+    the next linear: returns (codes int8 [M][K], sx fp32 [M][K/32]); residual_out and
+    y_out (fp16 [M][K]) are filled when given."""
+    M, K = x.shape
+    _need(x, torch.float16, (M, K), "x")
+    _need(gamma, torch.float16, (K,), "gamma")
+    for t, nm in ((residual, "residual"), (residual_out, "residual_out"), (y_out, "y_out")):
+        if t is not None:
+            _need(t, torch.float16, (M, K), nm)
+    if codes is None:
+        codes = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if sx is None:
+        sx = torch.empty((M, K // 32), dtype=torch.float32, device=x.device)
+    _need(codes, torch.int8, (M, K), "codes")
+    _need(sx, torch.float32, (M, K // 32), "sx")
+    _check(lib().w4a8_rmsnorm_quant(_p(x), _p(residual), _p(gamma), float(eps), M, K, _p(residual_out), _p(y_out),
+                                    _p(codes), _p(sx), _stream()), "w4a8_rmsnorm_quant")
+    return codes, sx
+
+
+def linear_q8(codes, sx, packed, scales, out=None, workspace=None):
+    """The linear on producer-quantised activations (codes int8 [M][K], sx fp32 [M][K/32])."""
+    M, K = codes.shape
+    N = scales.shape[0]
+    _need(codes, torch.int8, (M, K), "codes")
+    _need(sx, torch.float32, (M, K // 32), "sx")
+    _need(packed, torch.uint8, (N, K // 2), "packed")
+    _need(scales, torch.float16, (N, K // 32), "scales")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=codes.device)
+    _need(out, torch.float16, (M, N), "out")
+    need = lib().w4a8_linear_q8_workspace_bytes(M, N, K)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=codes.device)
+    wsb = workspace.numel() if workspace is not None else 0
+    _check(lib().w4a8_linear_q8(_p(codes), _p(sx), _p(packed), _p(scales), M, N, K, _p(out), _p(workspace), wsb,
+                                _stream()), "w4a8_linear_q8")
     return out
 
 

@@ -211,6 +211,36 @@ w4a8_status w4a8_linear_gated(const uint16_t *x, const void *packed_gu, const ui
     return launch_gated(x, packed_gu, scales_gu, M, N, K, out, act, workspace, workspace_bytes, stream);
 }
 
+w4a8_status w4a8_rmsnorm_quant(const uint16_t *x, const uint16_t *residual, const uint16_t *gamma, float eps,
+                               int M, int K, uint16_t *residual_out, uint16_t *y_out, int8_t *codes, float *sx,
+                               cudaStream_t stream) {
+    if (!shape_ok(M, 1, K) || !(eps >= 0.0f) || eps > 3.0e38f) return W4A8_ERR_INVALID_VALUE;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(codes) || !aligned16(sx)) return W4A8_ERR_MISALIGNED;
+    if ((residual && !aligned16(residual)) || (residual_out && !aligned16(residual_out)) || (y_out && !aligned16(y_out)))
+        return W4A8_ERR_MISALIGNED;
+    w4a8_status st = check_device();
+    if (st != W4A8_OK) return st;
+    cudaGetLastError();
+    return launch_rmsnorm_quant(x, residual, gamma, eps, M, K, residual_out, y_out, codes, sx, stream);
+}
+
+size_t w4a8_linear_q8_workspace_bytes(int M, int N, int K) {
+    if (!shape_ok(M, N, K)) return 0;
+    return q8_workspace_bytes(M, N, K);
+}
+
+w4a8_status w4a8_linear_q8(const int8_t *codes, const float *sx, const void *packed_w, const uint16_t *scales,
+                           int M, int N, int K, uint16_t *out, void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+    if (!shape_ok(M, N, K)) return W4A8_ERR_INVALID_VALUE;
+    if (!aligned16(codes) || !aligned16(sx) || !aligned16(packed_w) || !aligned16(scales) || !aligned16(out))
+        return W4A8_ERR_MISALIGNED;
+    w4a8_status st = check_device();
+    if (st != W4A8_OK) return st;
+    cudaGetLastError();
+    return launch_linear_q8(codes, sx, packed_w, scales, M, N, K, out, workspace, workspace_bytes, stream);
+}
+
 w4a8_status w4a8_debug_quantize_act(const uint16_t *x, int M, int K, int8_t *codes, float *sx,
                                     cudaStream_t stream) {
     if (!shape_ok(M, 1, K)) return W4A8_ERR_INVALID_VALUE;

@@ -575,12 +575,17 @@ w4a8_status launch_prefill(const uint16_t *x, const void *packed_w, const uint16
                            int M, int N, int K, uint16_t *out, int32_t *dots, void *workspace,
                            cudaStream_t stream) {
     const int mp = m_pad(M);
-    const int nb = K / 32;
     uint16_t *q16 = static_cast<uint16_t *>(workspace);
     float *sx = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + (size_t)mp * K * 2);
     w4a8_status st = launch_quant_prefill(x, M, K, mp, q16, sx, stream);
     if (st != W4A8_OK) return st;
+    return launch_prefill_gemm(q16, sx, packed_w, scales, M, N, K, out, dots, stream);
+}
 
+w4a8_status launch_prefill_gemm(const uint16_t *q16, const float *sx, const void *packed_w, const uint16_t *scales,
+                                int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream) {
+    const int mp = m_pad(M);
+    const int nb = K / 32;
     CUtensorMap ta, tw, ts;
     if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, q16, (uint64_t)K, (uint64_t)mp, 64, BN,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||

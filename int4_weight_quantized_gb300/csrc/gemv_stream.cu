@@ -58,6 +58,8 @@ struct StreamArgs {
     size_t stage_bytes;  // weights + scales per stage, 16-byte multiple
     int nslots;          // ring slots (<= STAGES)
     int act;             // gated kernel: 1 = SiLU, 2 = GELU (tanh form)
+    const int8_t *xq;    // Q8 input: activation codes [M][K] (natural k order) ...
+    const float *xs;     // ... and their block scales [M][K/32]
 };
 
 // Activation of the gated kernel's gate branch, from its definition:
@@ -116,9 +118,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 // the gate rows of the CTA's range and the matching up rows, and output row
 // n is act(gate_n . x) * (up_n . x) -- the element-wise operators of two
 // branches fused into the fully connected operator.
-template <int MT, int BPL, bool DEBUG, bool GATED>
+// Q8: the activations arrive already quantised (int8 codes and fp32 block
+// scales, e.g. from the RMS-normalisation operator) instead of as fp16 x.
+template <int MT, int BPL, bool DEBUG, bool GATED, bool Q8>
 __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
-    static_assert(!(DEBUG && GATED), "the debug instantiation is the plain linear");
+    static_assert(!(DEBUG && GATED) && !(DEBUG && Q8), "the debug instantiation is the plain linear");
     constexpr int NV = GATED ? 2 : 1;         // weight rows per output row
     constexpr int RG = (8 / MT) < RG_MAX ? (8 / MT) : RG_MAX;
     const int rgr = a.rg;
@@ -197,7 +201,27 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
                 const int rem = i - m * a.nb * 4;
                 b = rem >> 2;
                 t = rem & 3;
-                if (m < a.M) xv = *reinterpret_cast<const uint4 *>(a.x + (size_t)m * a.K + (size_t)b * kBlock + t * 8);
+                if (!Q8 && m < a.M) xv = *reinterpret_cast<const uint4 *>(a.x + (size_t)m * a.K + (size_t)b * kBlock + t * 8);
+            }
+            if constexpr (Q8) {
+                // 8 codes of this block: even k to one word, odd k to the other,
+                // as the quantiser below packs them; the block's code sum for
+                // the unsigned-weight offset comes from two dp4a with ones
+                uint2 cv = make_uint2(0u, 0u);
+                if (act) cv = *reinterpret_cast<const uint2 *>(a.xq + (size_t)m * a.K + (size_t)b * kBlock + t * 8);
+                int sum = __dp4a((int)cv.x, 0x01010101, __dp4a((int)cv.y, 0x01010101, 0));
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1, 4);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2, 4);
+                if (act) {
+                    uint32_t *cw = codes + ((size_t)m * a.nb + b) * 8;
+                    cw[2 * t] = __byte_perm(cv.x, cv.y, 0x6420);
+                    cw[2 * t + 1] = __byte_perm(cv.x, cv.y, 0x7531);
+                    if (t == 0) {
+                        sxs[m * a.nb + b] = a.xs[(size_t)m * a.nb + b];
+                        cbs[m * a.nb + b] = kMagicBits - 8 * sum;
+                    }
+                }
+                continue;
             }
             Quant8 r = quant8_group4(xv);
             if (act) {
@@ -417,9 +441,9 @@ Plan make_plan(int M, int N, int K, int nv = 1) {
     return p;
 }
 
-template <int MT, int BPL, bool DEBUG, bool GATED>
+template <int MT, int BPL, bool DEBUG, bool GATED, bool Q8>
 w4a8_status launch_t(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
-    auto kern = gemv_stream_kernel<MT, BPL, DEBUG, GATED>;
+    auto kern = gemv_stream_kernel<MT, BPL, DEBUG, GATED, Q8>;
     static int attr_done[64] = {};   // per device: the opt-in shared-memory limit is set once
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W4A8_ERR_CUDA;
@@ -445,32 +469,32 @@ w4a8_status launch_t(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
     return w4a8_host::launch_status();
 }
 
-template <bool DEBUG, bool GATED>
+template <bool DEBUG, bool GATED, bool Q8>
 w4a8_status dispatch(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
     switch (p.MT * 16 + p.BPL) {
-        case 1 * 16 + 1: return launch_t<1, 1, DEBUG, GATED>(p, a, stream);
-        case 1 * 16 + 2: return launch_t<1, 2, DEBUG, GATED>(p, a, stream);
-        case 1 * 16 + 4: return launch_t<1, 4, DEBUG, GATED>(p, a, stream);
-        case 1 * 16 + 8: return launch_t<1, 8, DEBUG, GATED>(p, a, stream);
-        case 2 * 16 + 1: return launch_t<2, 1, DEBUG, GATED>(p, a, stream);
-        case 2 * 16 + 2: return launch_t<2, 2, DEBUG, GATED>(p, a, stream);
-        case 2 * 16 + 4: return launch_t<2, 4, DEBUG, GATED>(p, a, stream);
-        case 3 * 16 + 1: return launch_t<3, 1, DEBUG, GATED>(p, a, stream);
-        case 3 * 16 + 2: return launch_t<3, 2, DEBUG, GATED>(p, a, stream);
-        case 4 * 16 + 1: return launch_t<4, 1, DEBUG, GATED>(p, a, stream);
-        case 4 * 16 + 2: return launch_t<4, 2, DEBUG, GATED>(p, a, stream);
-        case 5 * 16 + 1: return launch_t<5, 1, DEBUG, GATED>(p, a, stream);
-        case 6 * 16 + 1: return launch_t<6, 1, DEBUG, GATED>(p, a, stream);
-        case 7 * 16 + 1: return launch_t<7, 1, DEBUG, GATED>(p, a, stream);
-        case 8 * 16 + 1: return launch_t<8, 1, DEBUG, GATED>(p, a, stream);
-        case 1 * 16 + 0: return launch_t<1, 0, DEBUG, GATED>(p, a, stream);
-        case 2 * 16 + 0: return launch_t<2, 0, DEBUG, GATED>(p, a, stream);
-        case 3 * 16 + 0: return launch_t<3, 0, DEBUG, GATED>(p, a, stream);
-        case 4 * 16 + 0: return launch_t<4, 0, DEBUG, GATED>(p, a, stream);
-        case 5 * 16 + 0: return launch_t<5, 0, DEBUG, GATED>(p, a, stream);
-        case 6 * 16 + 0: return launch_t<6, 0, DEBUG, GATED>(p, a, stream);
-        case 7 * 16 + 0: return launch_t<7, 0, DEBUG, GATED>(p, a, stream);
-        case 8 * 16 + 0: return launch_t<8, 0, DEBUG, GATED>(p, a, stream);
+        case 1 * 16 + 1: return launch_t<1, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 1 * 16 + 2: return launch_t<1, 2, DEBUG, GATED, Q8>(p, a, stream);
+        case 1 * 16 + 4: return launch_t<1, 4, DEBUG, GATED, Q8>(p, a, stream);
+        case 1 * 16 + 8: return launch_t<1, 8, DEBUG, GATED, Q8>(p, a, stream);
+        case 2 * 16 + 1: return launch_t<2, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 2 * 16 + 2: return launch_t<2, 2, DEBUG, GATED, Q8>(p, a, stream);
+        case 2 * 16 + 4: return launch_t<2, 4, DEBUG, GATED, Q8>(p, a, stream);
+        case 3 * 16 + 1: return launch_t<3, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 3 * 16 + 2: return launch_t<3, 2, DEBUG, GATED, Q8>(p, a, stream);
+        case 4 * 16 + 1: return launch_t<4, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 4 * 16 + 2: return launch_t<4, 2, DEBUG, GATED, Q8>(p, a, stream);
+        case 5 * 16 + 1: return launch_t<5, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 6 * 16 + 1: return launch_t<6, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 7 * 16 + 1: return launch_t<7, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 8 * 16 + 1: return launch_t<8, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 1 * 16 + 0: return launch_t<1, 0, DEBUG, GATED, Q8>(p, a, stream);
+        case 2 * 16 + 0: return launch_t<2, 0, DEBUG, GATED, Q8>(p, a, stream);
+        case 3 * 16 + 0: return launch_t<3, 0, DEBUG, GATED, Q8>(p, a, stream);
+        case 4 * 16 + 0: return launch_t<4, 0, DEBUG, GATED, Q8>(p, a, stream);
+        case 5 * 16 + 0: return launch_t<5, 0, DEBUG, GATED, Q8>(p, a, stream);
+        case 6 * 16 + 0: return launch_t<6, 0, DEBUG, GATED, Q8>(p, a, stream);
+        case 7 * 16 + 0: return launch_t<7, 0, DEBUG, GATED, Q8>(p, a, stream);
+        case 8 * 16 + 0: return launch_t<8, 0, DEBUG, GATED, Q8>(p, a, stream);
         default: return W4A8_ERR_UNSUPPORTED;
     }
 }
@@ -489,7 +513,8 @@ bool gemv_stream_preferred(int M, int N, int K) {
 namespace {
 
 w4a8_status run_stream(const uint16_t *x, const void *packed_w, const uint16_t *scales, int M, int N, int K,
-                       uint16_t *out, int32_t *dots, int act, cudaStream_t stream) {
+                       uint16_t *out, int32_t *dots, int act, cudaStream_t stream,
+                       const int8_t *xq = nullptr, const float *xs = nullptr) {
     int *status = device_status_ptr();
     if (!status) return W4A8_ERR_CUDA;
     const bool gated = act != 0;
@@ -498,7 +523,9 @@ w4a8_status run_stream(const uint16_t *x, const void *packed_w, const uint16_t *
         Plan p = make_plan(mc, N, K, gated ? 2 : 1);
         if (!p.ok) return W4A8_ERR_UNSUPPORTED;
         StreamArgs a;
-        a.x = x + (size_t)m0 * K;
+        a.x = x ? x + (size_t)m0 * K : nullptr;
+        a.xq = xq ? xq + (size_t)m0 * K : nullptr;
+        a.xs = xs ? xs + (size_t)m0 * (K / 32) : nullptr;
         a.pw = static_cast<const uint8_t *>(packed_w);
         a.sw = scales;
         a.out = out + (size_t)m0 * N;
@@ -516,8 +543,9 @@ w4a8_status run_stream(const uint16_t *x, const void *packed_w, const uint16_t *
         a.stage_bytes = p.stage_bytes;
         a.nslots = p.nslots;
         a.act = act;
-        w4a8_status st = gated ? dispatch<false, true>(p, a, stream)
-                               : (dots ? dispatch<true, false>(p, a, stream) : dispatch<false, false>(p, a, stream));
+        w4a8_status st = gated ? dispatch<false, true, false>(p, a, stream)
+                         : xq ? dispatch<false, false, true>(p, a, stream)
+                         : (dots ? dispatch<true, false, false>(p, a, stream) : dispatch<false, false, false>(p, a, stream));
         if (st != W4A8_OK) return st;
     }
     return W4A8_OK;
@@ -528,6 +556,11 @@ w4a8_status run_stream(const uint16_t *x, const void *packed_w, const uint16_t *
 w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const uint16_t *scales,
                                int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream) {
     return run_stream(x, packed_w, scales, M, N, K, out, dots, 0, stream);
+}
+
+w4a8_status launch_gemv_stream_q8(const int8_t *codes, const float *sx, const void *packed_w, const uint16_t *scales,
+                                  int M, int N, int K, uint16_t *out, cudaStream_t stream) {
+    return run_stream(nullptr, packed_w, scales, M, N, K, out, nullptr, 0, stream, codes, sx);
 }
 
 bool gemv_stream_gated_supported(int M, int N, int K) { return make_plan(M < 8 ? M : 8, N, K, 2).ok; }

@@ -36,6 +36,10 @@ bool gemv_stream_supported(int M, int N, int K);
 bool gemv_stream_preferred(int M, int N, int K);
 // Gated pair (gate rows 0..N-1 over up rows N..2N-1 of one packed matrix):
 // out[m][n] = act(gate_n . x_m) * (up_n . x_m), act 1 = SiLU, 2 = GELU (tanh).
+// Decode GEMV on activations quantised by their producer: codes int8 [M][K]
+// (natural k order) and s_x fp32 [M][K/32].
+w4a8_status launch_gemv_stream_q8(const int8_t *codes, const float *sx, const void *packed_w, const uint16_t *scales,
+                                  int M, int N, int K, uint16_t *out, cudaStream_t stream);
 bool gemv_stream_gated_supported(int M, int N, int K);
 bool gemv_stream_gated_preferred(int M, int N, int K);
 w4a8_status launch_gemv_stream_gated(const uint16_t *x, const void *packed_gu, const uint16_t *scales_gu,
@@ -45,8 +49,23 @@ w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const ui
 
 // Prefill path: quantisation pass into `workspace`, then the tensor-core GEMM.
 size_t prefill_workspace_bytes(int M, int N, int K);
+// The GEMM alone, on activations already in the prefill layout: q16 fp16
+// codes [Mp][K] (k permuted 0,4,1,5,2,6,3,7 in every 8) and sx fp32 [K/32][Mp],
+// Mp = M rounded up to 128 (rows past M zero).
+w4a8_status launch_prefill_gemm(const uint16_t *q16, const float *sx, const void *packed_w, const uint16_t *scales,
+                                int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream);
+
 // CTAs along K per output tile of the prefill GEMM (1, 2, 4 or 8).
 int prefill_splits(int M, int N, int K);
+
+// RMS normalisation (+ residual) emitting activation codes (norm.cu), and the
+// linear on such codes (decode GEMV when it takes the shape, else conversion
+// to the prefill layout + the GEMM, in the workspace).
+w4a8_status launch_rmsnorm_quant(const uint16_t *x, const uint16_t *res, const uint16_t *gamma, float eps, int M, int K,
+                                 uint16_t *res_out, uint16_t *y_out, int8_t *codes, float *sx, cudaStream_t stream);
+size_t q8_workspace_bytes(int M, int N, int K);
+w4a8_status launch_linear_q8(const int8_t *codes, const float *sx, const void *packed_w, const uint16_t *scales, int M,
+                             int N, int K, uint16_t *out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 // The plain linear on the automatically chosen path (api.cu), and its
 // workspace size; used by the gated pair's unfused route.

@@ -171,6 +171,81 @@ def test_linear_gated_rejects_bad_act_and_missing_workspace(w4):
     assert st == 7   # W4A8_ERR_WORKSPACE
 
 
+# ------------------------------------------ producer-side quantisation
+
+def _fp16_ulp(v):
+    a = np.abs(v.astype(np.float32))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
+    return np.exp2(e - 10)
+
+
+NORM_SHAPES = [(1, 32), (3, 2048), (8, 4096), (5, 14336), (130, 320)]
+
+
+@pytest.mark.parametrize("with_res", [False, True])
+@pytest.mark.parametrize("M,K", NORM_SHAPES)
+def test_rmsnorm_quant(w4, M, K, with_res):
+    """Residual stream bit-exact; y (fp32 arithmetic here, fp64 in the oracle)
+    within one fp16 ulp; codes and scales bit-exact against the oracle's
+    quantiser applied to the kernel's own y (the decision is taken on the
+    same fp16 values on both sides)."""
+    g = np.random.default_rng(900 + M + K)
+    x = (g.standard_normal((M, K)) * 2).astype(np.float16)
+    res = g.standard_normal((M, K)).astype(np.float16) if with_res else None
+    gamma = g.uniform(0.5, 1.5, K).astype(np.float16)
+    eps = 1e-6
+    xd = torch.from_numpy(x).cuda()
+    rd = torch.from_numpy(res).cuda() if with_res else None
+    gd = torch.from_numpy(gamma).cuda()
+    ro = torch.empty_like(xd)
+    yo = torch.empty_like(xd)
+    codes, sx = w4.rmsnorm_quant(xd, gd, eps, residual=rd, residual_out=ro, y_out=yo)
+    r_ref, y_ref, q_ref, s_ref = oracle.rmsnorm_quant(x, res, gamma, eps)
+    assert np.array_equal(_np(ro).view(np.uint16), r_ref.view(np.uint16))
+    yg = _np(yo)
+    assert np.all(np.abs(yg.astype(np.float32) - y_ref.astype(np.float32)) <= _fp16_ulp(y_ref))
+    assert np.mean(yg == y_ref) > 0.95
+    qg, sg = oracle.quantize_act(yg)
+    assert np.array_equal(_np(codes), qg) and np.array_equal(_np(sx), sg)
+
+
+# (M, N, K, same kernel as the fp16 linear): codes input always decodes with
+# the streaming kernel, while the fp16 linear takes the cluster split-K
+# kernel for 3-8 tokens with long rows, whose summation order differs
+Q8_SHAPES = [(1, 512, 2048, True), (2, 300, 3072, True), (5, 257, 4096, False), (8, 129, 2048, False),
+             (9, 130, 512, True), (64, 96, 256, True), (200, 70, 320, True)]
+
+
+@pytest.mark.parametrize("M,N,K,same", Q8_SHAPES)
+def test_linear_q8_matches_linear(w4, M, N, K, same):
+    """The linear on producer codes matches the oracle within the fp16
+    tolerance, and gives exactly what the linear on the fp16 activations
+    gives when both run the same kernel after the quantisation step."""
+    x = wl.make_x(M, K, seed=1000 + M, outlier_frac=0.01)
+    codes, scales = wl.make_weights(N, K, seed=1100 + N, s_lo=0.002, s_hi=0.01)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    q, s = oracle.quantize_act(x.numpy())
+    y8 = w4.linear_q8(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), packed, sd)
+    y = w4.linear(xd, packed, sd)
+    torch.cuda.synchronize()
+    if same:
+        assert torch.equal(y8, y)
+    assert_fp16_close(_np(y8), oracle.linear(x.numpy(), codes.numpy(), scales.numpy()), f"q8 {M}x{N}x{K}")
+
+
+def test_rmsnorm_then_linear_q8(w4):
+    M, N, K = 1, 2048, 2048
+    g = np.random.default_rng(77)
+    x = g.standard_normal((M, K)).astype(np.float16)
+    gamma = g.uniform(0.5, 1.5, K).astype(np.float16)
+    codes_w, scales_w = wl.make_weights(N, K, seed=78, s_lo=0.002, s_hi=0.01)
+    packed = w4.pack(codes_w.cuda())
+    yo = torch.empty((M, K), dtype=torch.float16, device="cuda")
+    q, s = w4.rmsnorm_quant(torch.from_numpy(x).cuda(), torch.from_numpy(gamma).cuda(), 1e-6, y_out=yo)
+    out = w4.linear_q8(q, s, packed, scales_w.cuda())
+    assert_fp16_close(_np(out), oracle.linear(_np(yo), codes_w.numpy(), scales_w.numpy()), "norm+q8")
+
+
 # ---------------------------------------------------------------- linear
 
 EDGE_SHAPES = ([(M, 67, 160) for M in range(1, 10)] + [(15, 33, 64), (16, 256, 512), (17, 50, 96),
