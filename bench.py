@@ -44,9 +44,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only-secondary", action="store_true",
                     help="time only the secondary workloads and print their records")
-    ap.add_argument("--secondary", default="prefill,layers,sweep",
+    ap.add_argument("--secondary", default="prefill,layers,sweep,q8",
                     help="comma list of secondary workloads to run: prefill, layers (both layer "
-                         "workloads), layers_fused, sweep")
+                         "workloads), layers_fused, sweep, q8 (decode on producer-quantised activations)")
     return ap.parse_args()
 
 
@@ -289,6 +289,11 @@ def main():
             "note": "launch time = timed region / launches (every launch in the step is this kernel)"}
 
     # ---- end to end through the C entry point with pinned host buffers
+    # Every step copies the step's inputs from pinned host memory, runs the
+    # cps calls of w4a8_linear (the plain C entry point) and reads all outputs
+    # back, inside the timed region.  "graph": the calls are captured once
+    # into a CUDA graph, as a decode loop runs them; "eager": one Python call
+    # per linear (host-bound: ctypes and launch overhead per call).
     e2e_steps = max(3, min(args.steps, 50))
     xh = torch.empty((cps, lin.M, lin.K), dtype=torch.float16).pin_memory()
     xh.copy_(xs.cpu().expand(cps, lin.M, lin.K))
@@ -296,22 +301,35 @@ def main():
     xd = torch.empty((cps, lin.M, lin.K), dtype=torch.float16, device=dev)
     yd = torch.empty((cps, lin.M, lin.N), dtype=torch.float16, device=dev)
     with torch.cuda.stream(stream):
-        def e2e_step():
-            xd.copy_(xh, non_blocking=True)
+        def e2e_calls():
             for c in range(cps):
                 i = c % S
                 w4.linear_c(xd[c], sets[i][0], sets[i][1], yd[c])
+
+        def e2e_step(run):
+            xd.copy_(xh, non_blocking=True)
+            run()
             yh.copy_(yd, non_blocking=True)
             stream.synchronize()
-        e2e_step()
+        e2e_step(e2e_calls)
+        ge = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ge, stream=stream):
+            e2e_calls()
+        e2e_step(ge.replay)
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
-            e2e_step()
-        e2e_s = time.perf_counter() - t0
-    e2e_val = ws * bytes_step * e2e_steps / e2e_s / 1e9
-    e2e = {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": xh.numel() * 2,
-           "d2h_bytes_per_step": yh.numel() * 2, "steps": e2e_steps,
-           "note": "w4a8_linear per call, eager launches, inputs copied from pinned host each step, outputs read back"}
+            e2e_step(ge.replay)
+        e2e_graph_s = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step(e2e_calls)
+        e2e_eager_s = time.perf_counter() - t0
+    e2e = {"value": ws * bytes_step * e2e_steps / e2e_graph_s / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": yh.numel() * 2, "steps": e2e_steps,
+           "note": "host wall clock per step: pinned x -> device, CUDA graph of the step's w4a8_linear calls, "
+                   "all y -> pinned host, synchronize",
+           "eager_value": ws * bytes_step * e2e_steps / e2e_eager_s / 1e9,
+           "eager_note": "same step with one Python/ctypes w4a8_linear call per linear (host-bound)"}
 
     secondary = []
     if not args.no_secondary:
@@ -338,7 +356,7 @@ def main():
         dist.destroy_process_group()
 
 
-def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, which="prefill,layers,sweep"):
+def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, which="prefill,layers,sweep,q8"):
     """Secondary workloads: prefill GEMM (M=512) in TOPS, the 26-layer decode
     step and the shape sweep, each timed with CUDA events on its stream."""
     import torch
@@ -352,7 +370,57 @@ def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, which="prefill,layer
         res.append(run_decoder_layers(w4, wl, dev, stream, hbm, peak_src, name="decoder_layers_m1_26x4_fused"))
     if "sweep" in which:
         res.append(run_sweep(w4, wl, dev, stream, hbm, bf16, peak_src))
+    if "q8" in which:
+        res.append(run_decode_q8(w4, wl, dev, stream, hbm, peak_src))
     return res
+
+
+def run_decode_q8(w4, wl, dev, stream, hbm, peak_src, cps=512, sets=16, steps=20):
+    """The headline decode shape (M=1, K=2048, N=8192, 16 rotating weight sets)
+    on activations quantised by their producer (w4a8_linear_q8: int8 codes and
+    fp32 block scales in, no in-kernel quantisation), beside the fp16-input
+    linear timed the same way; plus the producer itself (w4a8_rmsnorm_quant)
+    followed by the linear.  CUDA graphs of cps calls."""
+    import torch
+    W = [w for w in wl.workloads() if w.name == HEADLINE][0]
+    lin = W.linears[0]
+    xs = wl.make_x(lin.M, lin.K, W.seed, lin.outlier_frac).to(dev)
+    gamma = torch.ones(lin.K, dtype=torch.float16, device=dev)
+    wsets = []
+    for i in range(sets):
+        c, s = wl.make_weights(lin.N, lin.K, W.seed + 1 + i, lin.s_lo, lin.s_hi)
+        wsets.append((w4.pack(c.to(dev)), s.to(dev)))
+    out = torch.empty((lin.M, lin.N), dtype=torch.float16, device=dev)
+    with torch.cuda.stream(stream):
+        q, sx = w4.rmsnorm_quant(xs, gamma, 1e-6)
+
+        def timed(body):
+            body()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                body()
+            for _ in range(3):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1) * 1e-3 / (steps * cps)
+
+        t_q8 = timed(lambda: [w4.linear_q8(q, sx, *wsets[c % sets], out=out) for c in range(cps)])
+        t_fp16 = timed(lambda: [w4.linear(xs, *wsets[c % sets], out=out, path=w4.PATH_DECODE) for c in range(cps)])
+        t_norm = timed(lambda: [(w4.rmsnorm_quant(xs, gamma, 1e-6, codes=q, sx=sx),
+                                 w4.linear_q8(q, sx, *wsets[c % sets], out=out)) for c in range(cps)])
+    byt = lin.weight_bytes + lin.M * lin.K + lin.M * (lin.K // 32) * 4 + 2 * lin.M * lin.N
+    return {"workload": "decode_ffn_up_q8_m1_k2048_n8192", "value": byt / t_q8 / 1e9, "unit": "GB/s",
+            "us_per_call": t_q8 * 1e6, "fp16_input_us_per_call": t_fp16 * 1e6,
+            "rmsnorm_quant_plus_linear_us": t_norm * 1e6,
+            "roofline": {"bound": "hbm", "achieved": byt / t_q8 / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": byt / t_q8 / 1e9 / hbm, "peak_source": peak_src},
+            "note": "bytes = int4 weights + fp16 scales + int8 codes + fp32 block scales + fp16 y"}
 
 
 def run_prefill(w4, wl, dev, stream, bf16, peak_src):

@@ -208,7 +208,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
                 // as the quantiser below packs them; the block's code sum for
                 // the unsigned-weight offset comes from two dp4a with ones
                 uint2 cv = make_uint2(0u, 0u);
-                if (act) cv = *reinterpret_cast<const uint2 *>(a.xq + (size_t)m * a.K + (size_t)b * kBlock + t * 8);
+                float sxv = 0.0f;
+                if (act) {
+                    // both loads in flight together: the scale does not wait for the code sums
+                    cv = *reinterpret_cast<const uint2 *>(a.xq + (size_t)m * a.K + (size_t)b * kBlock + t * 8);
+                    if (t == 0) sxv = a.xs[(size_t)m * a.nb + b];
+                }
                 int sum = __dp4a((int)cv.x, 0x01010101, __dp4a((int)cv.y, 0x01010101, 0));
                 sum += __shfl_xor_sync(0xffffffffu, sum, 1, 4);
                 sum += __shfl_xor_sync(0xffffffffu, sum, 2, 4);
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
                     cw[2 * t] = __byte_perm(cv.x, cv.y, 0x6420);
                     cw[2 * t + 1] = __byte_perm(cv.x, cv.y, 0x7531);
                     if (t == 0) {
-                        sxs[m * a.nb + b] = a.xs[(size_t)m * a.nb + b];
+                        sxs[m * a.nb + b] = sxv;
                         cbs[m * a.nb + b] = kMagicBits - 8 * sum;
                     }
                 }
