@@ -37,9 +37,11 @@ class Oracle:
         L.oracle_linear_f64.argtypes = [P, P, P, i, i, i, P]
         L.oracle_linear_gated.argtypes = [P, P, P, i, i, i, i, P]
         L.oracle_rmsnorm_quant.argtypes = [P, P, P, ctypes.c_float, i, i, P, P, P, P]
+        L.oracle_decode_attention.argtypes = [P, P, P, P, i, i, i, i, i, P]
         L.oracle_unpack_weights.argtypes = [P, i, i, P]
         for f in ("oracle_quantize_act", "oracle_block_dots", "oracle_linear",
-                  "oracle_linear_f64", "oracle_linear_gated", "oracle_rmsnorm_quant", "oracle_unpack_weights"):
+                  "oracle_linear_f64", "oracle_linear_gated", "oracle_rmsnorm_quant", "oracle_decode_attention",
+                  "oracle_unpack_weights"):
             getattr(L, f).restype = ctypes.c_int
         self.L = L
         self.path = path
@@ -111,6 +113,19 @@ class Oracle:
                                            _ptr(sx)), "rmsnorm_quant")
         return ro, y, q, sx
 
+    def decode_attention(self, q, k, v, lens):
+        """q fp16 [B][Hq][D], k/v fp16 [B][Hkv][Lmax][D], lens int [B] -> out fp16 [B][Hq][D]."""
+        q = np.ascontiguousarray(q, np.float16)
+        k = np.ascontiguousarray(k, np.float16)
+        v = np.ascontiguousarray(v, np.float16)
+        lens = np.ascontiguousarray(lens, np.int32)
+        B, Hq, D = q.shape
+        Hkv, Lmax = k.shape[1], k.shape[2]
+        out = np.empty((B, Hq, D), np.float16)
+        _check(self.L.oracle_decode_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(lens), B, Hq, Hkv, D, Lmax, _ptr(out)),
+               "decode_attention")
+        return out
+
     def linear_f64(self, x, w, sw):
         """fp64 dequantise-then-multiply of the same codes and scales -> float64 [M][N]."""
         x = np.ascontiguousarray(x, np.float16)
@@ -165,6 +180,10 @@ def linear_gated(x, w, sw, act):
 
 def rmsnorm_quant(x, res, gamma, eps):
     return get().rmsnorm_quant(x, res, gamma, eps)
+
+
+def decode_attention(q, k, v, lens):
+    return get().decode_attention(q, k, v, lens)
 
 
 def unpack_weights(packed, N, K):

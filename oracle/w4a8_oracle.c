@@ -232,6 +232,48 @@ int oracle_rmsnorm_quant(const uint16_t *x, const uint16_t *res, const uint16_t 
     return rc;
 }
 
+/* ---- decode attention (softmax(q K^T / sqrt(D)) V, grouped heads) ---- */
+
+int oracle_decode_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *lens,
+                            int B, int Hq, int Hkv, int D, int Lmax, uint16_t *out)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || Lmax <= 0) return -1;
+    for (int b = 0; b < B; ++b)
+        if (lens[b] < 1 || lens[b] > Lmax) return -2;
+    int G = Hq / Hkv;
+    double scale = 1.0 / sqrt((double)D);
+    double *s = (double *)malloc(sizeof(double) * (size_t)Lmax);
+    double *o = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!s || !o) { free(s); free(o); return -4; }
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < Hq; ++h) {
+            int g = h / G, L = lens[b];
+            const uint16_t *qh = q + ((size_t)b * Hq + h) * D;
+            const uint16_t *kb = k + ((size_t)b * Hkv + g) * (size_t)Lmax * D;
+            const uint16_t *vb = v + ((size_t)b * Hkv + g) * (size_t)Lmax * D;
+            double m = -INFINITY;
+            for (int t = 0; t < L; ++t) {
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d)
+                    acc += (double)oracle_half_to_float(qh[d]) * (double)oracle_half_to_float(kb[(size_t)t * D + d]);
+                s[t] = acc * scale;
+                if (s[t] > m) m = s[t];
+            }
+            double den = 0.0;
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            for (int t = 0; t < L; ++t) {
+                double p = exp(s[t] - m);
+                den += p;
+                for (int d = 0; d < D; ++d) o[d] += p * (double)oracle_half_to_float(vb[(size_t)t * D + d]);
+            }
+            for (int d = 0; d < D; ++d)
+                out[((size_t)b * Hq + h) * D + d] = oracle_float_to_half((float)(o[d] / den));
+        }
+    free(s);
+    free(o);
+    return 0;
+}
+
 int oracle_linear_f64(const uint16_t *x, const int8_t *w, const uint16_t *sw,
                       int M, int N, int K, double *ref)
 {

@@ -77,6 +77,18 @@ int oracle_linear_gated(const uint16_t *x, const int8_t *w, const uint16_t *sw,
 int oracle_rmsnorm_quant(const uint16_t *x, const uint16_t *res, const uint16_t *gamma, float eps,
                          int M, int K, uint16_t *res_out, uint16_t *y, int8_t *q, float *sx);
 
+/* Decode attention over an fp16 KV cache (one new token per sequence), the
+ * other decode hot spot beside the linears ("Що змінює ML Drift для
+ * on-device AI-інференсу на вашому телефоні?", tech.dede.sh, section
+ * "Stage-aware оптимізація для великих мовних моделей": KV cache in decode).
+ * Grouped query heads: query head h reads KV head h / (Hq / Hkv).
+ *   q   [B][Hq][D] fp16        k, v [B][Hkv][Lmax][D] fp16 (rows t >= lens[b] unused)
+ *   lens [B], 1 <= lens[b] <= Lmax
+ *   s_t = (q . k_t) / sqrt(D),  out = sum_t softmax(s)_t v_t   (all in fp64)
+ *   out [B][Hq][D] fp16, rounded from fp64 through fp32. */
+int oracle_decode_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *lens,
+                            int B, int Hq, int Hkv, int D, int Lmax, uint16_t *out);
+
 /* Checker: the same dequantised product in fp64,
  * ref[m][n] = sum_b sum_k (double)sw*w * (double)sx*q, with the codes and
  * activation scales of oracle_quantize_act. */

@@ -410,4 +410,71 @@ def pin_rmsnorm_invariants(orc):
     assert np.array_equal(qa, q) and np.array_equal(sa, sx)
 
 
+def pin_attention_single_and_uniform(orc):
+    """One cached token: softmax weight 1, so out = v_0 exactly.  All keys
+    equal: uniform weights, so out = the mean of the value rows."""
+    rng = _rng(51)
+    B, Hq, Hkv, D, Lmax = 2, 4, 2, 64, 9
+    q = rng.standard_normal((B, Hq, D)).astype(np.float16)
+    k = rng.standard_normal((B, Hkv, Lmax, D)).astype(np.float16)
+    v = rng.standard_normal((B, Hkv, Lmax, D)).astype(np.float16)
+    out = orc.decode_attention(q, k, v, np.array([1, 1], np.int32))
+    for b in range(B):
+        for h in range(Hq):
+            assert np.array_equal(out[b, h].view(np.uint16), v[b, h // 2, 0].view(np.uint16))
+    ke = np.repeat(k[:, :, :1, :], Lmax, axis=2)
+    out = orc.decode_attention(q, ke, v, np.array([Lmax, 5], np.int32))
+    for b, L in ((0, Lmax), (1, 5)):
+        for h in range(Hq):
+            mean = v[b, h // 2, :L].astype(np.float64).mean(axis=0)
+            assert np.array_equal(out[b, h].view(np.uint16), mean.astype(np.float32).astype(np.float16).view(np.uint16))
+
+
+def pin_attention_group_mapping_and_lengths(orc):
+    """Query head h reads KV head h / (Hq/Hkv): with constant value rows 1,2,3
+    per KV head the outputs are those constants; rows past lens[b] never
+    matter (filled with huge values here)."""
+    B, Hq, Hkv, D, Lmax = 1, 6, 3, 32, 7
+    rng = _rng(53)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float16)
+    k = rng.standard_normal((B, Hkv, Lmax, D)).astype(np.float16)
+    v = np.zeros((B, Hkv, Lmax, D), np.float16)
+    for g in range(Hkv):
+        v[0, g] = g + 1
+    L = 4
+    k[0, :, L:] = 30000.0
+    v[0, :, L:] = -30000.0
+    out = orc.decode_attention(q, k, v, np.array([L], np.int32))
+    for h in range(Hq):
+        assert np.all(out[0, h] == (h // 2) + 1)
+
+
+def pin_attention_two_keys_closed_form(orc):
+    """Two cached tokens, q = e_0 * a, k_0 = e_0, k_1 = 0: scores a/sqrt(D) and
+    0, so with v_0 = 1 and v_1 = 0 the output is the logistic 1/(1+e^-s);
+    and a dominant key (score gap > 40) returns its value row exactly, even
+    where exp of the raw score would overflow (the max is subtracted first)."""
+    import math
+    D = 64
+    for a in (1.0, 4.0, -6.0, 20.0):
+        q = np.zeros((1, 1, D), np.float16)
+        q[0, 0, 0] = a
+        k = np.zeros((1, 1, 2, D), np.float16)
+        k[0, 0, 0, 0] = 1.0
+        v = np.zeros((1, 1, 2, D), np.float16)
+        v[0, 0, 0] = 1.0
+        out = orc.decode_attention(q, k, v, np.array([2], np.int32)).astype(np.float64)
+        s = a / math.sqrt(D)
+        want = 1.0 / (1.0 + math.exp(-s))
+        assert np.all(np.abs(out[0, 0] - want) <= 2.0 ** -11 * max(want, 2.0 ** -14))
+    rng = _rng(57)
+    q = np.zeros((1, 1, D), np.float16)
+    q[0, 0, :] = 1.0
+    k = (rng.standard_normal((1, 1, 5, D)) * 0.1).astype(np.float16)
+    k[0, 0, 3, :] = 120.0     # score 120*64/8 = 960: far above the rest (|s| < 8), and past exp's fp64 range
+    v = rng.standard_normal((1, 1, 5, D)).astype(np.float16)
+    out = orc.decode_attention(q, k, v, np.array([5], np.int32))
+    assert np.array_equal(out[0, 0].view(np.uint16), v[0, 0, 3].view(np.uint16))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -52,6 +52,11 @@ MUTANTS = [
      "double v = (double)r[k] * inv;"),
     ("rmsnorm_residual_dropped", "if (res) h = h + oracle_half_to_float(res[(size_t)m * K + k]);", "(void)res;"),
     ("rmsnorm_no_root", "double inv = 1.0 / sqrt(ms + (double)eps);", "double inv = 1.0 / (ms + (double)eps);"),
+    ("attention_scale_over_d", "double scale = 1.0 / sqrt((double)D);", "double scale = 1.0 / (double)D;"),
+    ("attention_group_modulo", "int g = h / G, L = lens[b];", "int g = h % Hkv, L = lens[b];"),
+    ("attention_length_off_by_one", "for (int t = 0; t < L; ++t) {\n                double p", "for (int t = 0; t <= L && t < Lmax; ++t) {\n                double p"),
+    ("attention_unnormalised", "(float)(o[d] / den)", "(float)(o[d])"),
+    ("attention_no_max_shift", "double p = exp(s[t] - m);", "double p = exp(s[t]);"),
     ("f64_drops_weight_scale", "acc += (swd * (double)w[(size_t)n * K + k]) * (sxd * (double)q[k]);",
      "acc += ((double)w[(size_t)n * K + k]) * (sxd * (double)q[k]);"),
 ]
