@@ -44,9 +44,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only-secondary", action="store_true",
                     help="time only the secondary workloads and print their records")
-    ap.add_argument("--secondary", default="prefill,layers,sweep,q8",
+    ap.add_argument("--secondary", default="prefill,layers,sweep,q8,attention",
                     help="comma list of secondary workloads to run: prefill, layers (both layer "
-                         "workloads), layers_fused, sweep, q8 (decode on producer-quantised activations)")
+                         "workloads), layers_fused, sweep, q8 (decode on producer-quantised activations), "
+                         "attention (decode attention over an fp16 KV cache)")
     return ap.parse_args()
 
 
@@ -356,7 +357,7 @@ def main():
         dist.destroy_process_group()
 
 
-def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, which="prefill,layers,sweep,q8"):
+def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, which="prefill,layers,sweep,q8,attention"):
     """Secondary workloads: prefill GEMM (M=512) in TOPS, the 26-layer decode
     step and the shape sweep, each timed with CUDA events on its stream."""
     import torch
@@ -372,7 +373,48 @@ def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, which="prefill,layer
         res.append(run_sweep(w4, wl, dev, stream, hbm, bf16, peak_src))
     if "q8" in which:
         res.append(run_decode_q8(w4, wl, dev, stream, hbm, peak_src))
+    if "attention" in which:
+        res.append(run_attention(w4, dev, stream, hbm, peak_src))
     return res
+
+
+def run_attention(w4, dev, stream, hbm, peak_src, B=32, Hq=8, Hkv=1, D=256, L=640, sets=8, cps=64, steps=20):
+    """Decode attention for B sequences of L = 640 cached tokens (prefill 512 +
+    128 decode steps) with the decoder layer's 8 query heads over one KV head of
+    256; 8 rotating caches (168 MB > L2); GB/s of K + V + q + out."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(6000)
+    caches = [(torch.randn((B, Hkv, L, D), generator=g, device=dev, dtype=torch.float32).half(),
+               torch.randn((B, Hkv, L, D), generator=g, device=dev, dtype=torch.float32).half()) for _ in range(sets)]
+    q = torch.randn((B, Hq, D), generator=g, device=dev, dtype=torch.float32).half()
+    lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+    out = torch.empty((B, Hq, D), dtype=torch.float16, device=dev)
+    ws = torch.empty(max(1, w4.lib().w4a8_decode_attention_workspace_bytes(B, Hq, Hkv, D, L)), dtype=torch.uint8,
+                     device=dev)
+    with torch.cuda.stream(stream):
+        def calls():
+            for c in range(cps):
+                k, v = caches[c % sets]
+                w4.decode_attention(q, k, v, lens, out=out, workspace=ws)
+        calls()
+        stream.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            calls()
+        for _ in range(3):
+            gr.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            gr.replay()
+        e1.record(stream)
+        e1.synchronize()
+    per = e0.elapsed_time(e1) * 1e-3 / (steps * cps)
+    byt = 2 * B * Hkv * L * D * 2 + 2 * 2 * B * Hq * D
+    return {"workload": f"decode_attention_b{B}_hq{Hq}_hkv{Hkv}_d{D}_l{L}", "value": byt / per / 1e9, "unit": "GB/s",
+            "us_per_call": per * 1e6,
+            "roofline": {"bound": "hbm", "achieved": byt / per / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": byt / per / 1e9 / hbm, "peak_source": peak_src}}
 
 
 def run_decode_q8(w4, wl, dev, stream, hbm, peak_src, cps=512, sets=16, steps=20):

@@ -187,6 +187,26 @@ w4a8_status w4a8_linear_q8(const int8_t *codes, const float *sx, const void *pac
                            int M, int N, int K, uint16_t *out, void *workspace, size_t workspace_bytes,
                            cudaStream_t stream);
 
+/* Decode attention over an fp16 KV cache, one new token per sequence (the
+ * other decode hot spot beside the linears; "Що змінює ML Drift для
+ * on-device AI-інференсу на вашому телефоні?", tech.dede.sh, section
+ * "Stage-aware оптимізація для великих мовних моделей").
+ *   q        [B][Hq][D] fp16, device
+ *   k_cache, v_cache  [B][Hkv][Lmax][D] fp16, device (this library's layout);
+ *            row t of sequence b is used for t < lens[b]
+ *   lens     [B] int32, device; values are clamped to [0, Lmax] (a sequence
+ *            of length 0 gets zeros)
+ *   out      [B][Hq][D] fp16:  out[b][h] = sum_t softmax_t(q.k_t / sqrt(D)) v_t,
+ *            KV head h / (Hq/Hkv) for query head h, fp32 arithmetic.
+ * Requires D in {64, 128, 256}, Hq % Hkv == 0, Hq/Hkv <= 16 and
+ * Lmax <= 131072, else W4A8_ERR_INVALID_VALUE.  Sequences longer than 128 tokens are split into
+ * 128-token chunks whose partial softmax sums are merged by a second kernel
+ * in `workspace` (w4a8_decode_attention_workspace_bytes; 0 when none). */
+size_t w4a8_decode_attention_workspace_bytes(int B, int Hq, int Hkv, int D, int Lmax);
+w4a8_status w4a8_decode_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                  const int32_t *lens, int B, int Hq, int Hkv, int D, int Lmax, uint16_t *out,
+                                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Debug: the activation quantiser alone, through the same device routine
  * the linear kernels use.  codes [M][K] int8 and sx [M][K/32] fp32, device. */
 w4a8_status w4a8_debug_quantize_act(const uint16_t *x, int M, int K, int8_t *codes,

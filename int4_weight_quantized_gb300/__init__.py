@@ -60,6 +60,9 @@ def lib():
         L.w4a8_linear_q8_workspace_bytes.argtypes = [i, i, i]
         L.w4a8_linear_q8_workspace_bytes.restype = sz
         L.w4a8_linear_q8.argtypes = [P, P, P, P, i, i, i, P, P, sz, P]
+        L.w4a8_decode_attention_workspace_bytes.argtypes = [i, i, i, i, i]
+        L.w4a8_decode_attention_workspace_bytes.restype = sz
+        L.w4a8_decode_attention.argtypes = [P, P, P, P, i, i, i, i, i, P, P, sz, P]
         L.w4a8_workspace_bytes.argtypes = [i, i, i, i]
         L.w4a8_workspace_bytes.restype = sz
         L.w4a8_linear.argtypes = [P, P, P, i, i, i, P, P]
@@ -71,7 +74,7 @@ def lib():
         L.w4a8_set_wait_budget.argtypes = [ctypes.c_longlong]
         L.w4a8_debug_wait_timeout.argtypes = [P]
         for f in ("w4a8_pack", "w4a8_linear", "w4a8_linear_ex", "w4a8_linear_gated", "w4a8_rmsnorm_quant",
-                  "w4a8_linear_q8", "w4a8_linear_prefill_noalloc", "w4a8_debug_quantize_act",
+                  "w4a8_linear_q8", "w4a8_decode_attention", "w4a8_linear_prefill_noalloc", "w4a8_debug_quantize_act",
                   "w4a8_debug_block_dots", "w4a8_get_device_status", "w4a8_set_wait_budget",
                   "w4a8_debug_wait_timeout"):
             getattr(L, f).restype = i
@@ -227,6 +230,27 @@ def linear_q8(codes, sx, packed, scales, out=None, workspace=None):
     wsb = workspace.numel() if workspace is not None else 0
     _check(lib().w4a8_linear_q8(_p(codes), _p(sx), _p(packed), _p(scales), M, N, K, _p(out), _p(workspace), wsb,
                                 _stream()), "w4a8_linear_q8")
+    return out
+
+
+def decode_attention(q, k_cache, v_cache, lens, out=None, workspace=None):
+    """Decode attention: q fp16 [B][Hq][D], caches fp16 [B][Hkv][Lmax][D], lens int32 [B]
+    (device) -> fp16 [B][Hq][D] (w4a8_decode_attention)."""
+    B, Hq, D = q.shape
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    _need(q, torch.float16, (B, Hq, D), "q")
+    _need(k_cache, torch.float16, (B, Hkv, Lmax, D), "k_cache")
+    _need(v_cache, torch.float16, (B, Hkv, Lmax, D), "v_cache")
+    _need(lens, torch.int32, (B,), "lens")
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=q.device)
+    _need(out, torch.float16, (B, Hq, D), "out")
+    need = lib().w4a8_decode_attention_workspace_bytes(B, Hq, Hkv, D, Lmax)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wsb = workspace.numel() if workspace is not None else 0
+    _check(lib().w4a8_decode_attention(_p(q), _p(k_cache), _p(v_cache), _p(lens), B, Hq, Hkv, D, Lmax, _p(out),
+                                       _p(workspace), wsb, _stream()), "w4a8_decode_attention")
     return out
 
 

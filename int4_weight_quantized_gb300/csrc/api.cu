@@ -241,6 +241,23 @@ w4a8_status w4a8_linear_q8(const int8_t *codes, const float *sx, const void *pac
     return launch_linear_q8(codes, sx, packed_w, scales, M, N, K, out, workspace, workspace_bytes, stream);
 }
 
+size_t w4a8_decode_attention_workspace_bytes(int B, int Hq, int Hkv, int D, int Lmax) {
+    if (!attention_shape_ok(B, Hq, Hkv, D, Lmax)) return 0;
+    return attention_workspace_bytes(B, Hq, D, Lmax);
+}
+
+w4a8_status w4a8_decode_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                  const int32_t *lens, int B, int Hq, int Hkv, int D, int Lmax, uint16_t *out,
+                                  void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!attention_shape_ok(B, Hq, Hkv, D, Lmax)) return W4A8_ERR_INVALID_VALUE;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(lens) || !aligned16(out))
+        return W4A8_ERR_MISALIGNED;
+    w4a8_status st = check_device();
+    if (st != W4A8_OK) return st;
+    cudaGetLastError();
+    return launch_attention(q, k_cache, v_cache, lens, B, Hq, Hkv, D, Lmax, out, workspace, workspace_bytes, stream);
+}
+
 w4a8_status w4a8_debug_quantize_act(const uint16_t *x, int M, int K, int8_t *codes, float *sx,
                                     cudaStream_t stream) {
     if (!shape_ok(M, 1, K)) return W4A8_ERR_INVALID_VALUE;

@@ -67,6 +67,13 @@ size_t q8_workspace_bytes(int M, int N, int K);
 w4a8_status launch_linear_q8(const int8_t *codes, const float *sx, const void *packed_w, const uint16_t *scales, int M,
                              int N, int K, uint16_t *out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+// Decode attention over an fp16 KV cache (attention.cu).
+bool attention_shape_ok(int B, int Hq, int Hkv, int D, int Lmax);
+size_t attention_workspace_bytes(int B, int Hq, int D, int Lmax);
+w4a8_status launch_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *lens, int B, int Hq,
+                             int Hkv, int D, int Lmax, uint16_t *out, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
+
 // The plain linear on the automatically chosen path (api.cu), and its
 // workspace size; used by the gated pair's unfused route.
 size_t linear_workspace_bytes(int M, int N, int K);

@@ -246,6 +246,45 @@ def test_rmsnorm_then_linear_q8(w4):
     assert_fp16_close(_np(out), oracle.linear(_np(yo), codes_w.numpy(), scales_w.numpy()), "norm+q8")
 
 
+# ---------------------------------------------------------- decode attention
+
+# (B, Hq, Hkv, D, Lmax, lens): the decoder layer's 8 query heads over one KV
+# head of 256 (5 chunks of 128), ragged lengths incl. 1 and a chunk edge, one
+# chunk (direct write, no combine), 16 heads per group with D=64, 3 KV heads,
+# group sizes 3 and 5 (not powers of two)
+ATTN_CASES = [(1, 8, 1, 256, 640, [640]), (3, 8, 1, 256, 200, [1, 129, 200]), (2, 4, 2, 128, 128, [128, 64]),
+              (4, 16, 1, 64, 300, [300, 1, 257, 128]), (2, 6, 3, 128, 1000, [999, 500]),
+              (2, 6, 2, 256, 130, [130, 3]), (1, 5, 1, 64, 64, [64])]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,Lmax,lens", ATTN_CASES)
+def test_decode_attention(w4, B, Hq, Hkv, D, Lmax, lens):
+    g = np.random.default_rng(1300 + B * Lmax + D)
+    q = g.standard_normal((B, Hq, D)).astype(np.float16)
+    k = g.standard_normal((B, Hkv, Lmax, D)).astype(np.float16)
+    v = g.standard_normal((B, Hkv, Lmax, D)).astype(np.float16)
+    ln = np.array(lens, np.int32)
+    out = w4.decode_attention(torch.from_numpy(q).cuda(), torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                              torch.from_numpy(ln).cuda())
+    ref = oracle.decode_attention(q, k, v, ln)
+    assert_fp16_close(_np(out).reshape(B * Hq, D), ref.reshape(B * Hq, D), f"attention {B},{Hq},{Hkv},{D},{Lmax}")
+
+
+def test_decode_attention_edge_lengths(w4):
+    """Lengths are clamped to [0, Lmax]: 0 gives zeros, more than Lmax reads Lmax rows."""
+    B, Hq, Hkv, D, Lmax = 3, 4, 1, 64, 300
+    g = np.random.default_rng(1400)
+    q = g.standard_normal((B, Hq, D)).astype(np.float16)
+    k = g.standard_normal((B, Hkv, Lmax, D)).astype(np.float16)
+    v = g.standard_normal((B, Hkv, Lmax, D)).astype(np.float16)
+    ln = np.array([0, 100000, 7], np.int32)
+    out = _np(w4.decode_attention(torch.from_numpy(q).cuda(), torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                                  torch.from_numpy(ln).cuda()))
+    assert not np.any(out[0].astype(np.float32))
+    ref = oracle.decode_attention(q[1:], k[1:], v[1:], np.array([Lmax, 7], np.int32))
+    assert_fp16_close(out[1:].reshape(-1, D), ref.reshape(-1, D), "clamped lengths")
+
+
 # ---------------------------------------------------------------- linear
 
 EDGE_SHAPES = ([(M, 67, 160) for M in range(1, 10)] + [(15, 33, 64), (16, 256, 512), (17, 50, 96),
