@@ -6,8 +6,11 @@ distinct weight sets (151 MB of packed weights and scales, more than the
 A step is one CUDA-graph replay of `--calls-per-step` consecutive decode
 calls cycling through the 16 sets.  The metric is effective HBM bandwidth:
 algorithmic bytes (int4 weights + fp16 block scales + fp16 x + fp16 y) per
-second.  Secondary lines in the same JSON record the prefill GEMM
-(M=512, K=2048, N=8192) in int8-equivalent TOPS (2*M*N*K per call).
+second.  Secondary records in the same JSON line (`--secondary`): the
+prefill GEMM (M=512, K=2048, N=8192) in int8-equivalent TOPS (2*M*N*K per
+call), one decode step over 26 decoder layers (7 linears per layer, and the
+fused layer: q/k/v as one projection, gated gate/up, down), a shape sweep,
+the decode linear on producer-quantised activations, and decode attention.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs an independent replica (the linear has no
@@ -285,7 +288,7 @@ def main():
     achieved = lin.bytes / per_launch_s / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": traffic_for("gemv_stream_decode_ffn_up", gemv_files), "peak_source": peak_src,
-            "kernel": "gemv_stream_kernel<1,2,false>", "algorithmic_bytes_per_launch": lin.bytes,
+            "kernel": "gemv_stream_kernel<1,2,false,false,false>", "algorithmic_bytes_per_launch": lin.bytes,
             "launch_time_us": per_launch_s * 1e6,
             "note": "launch time = timed region / launches (every launch in the step is this kernel)"}
 
@@ -551,7 +554,7 @@ def run_sweep(w4, wl, dev, stream, hbm, bf16, peak_src, sets=5, reps=20):
                          "frac_hbm": gbs / hbm, "frac_fp16_tensor": tops / bf16})
             del ws
     return {"workload": W.name, "rows": rows, "peak_source": peak_src,
-            "note": "decode rows are judged on GB/s against HBM, prefill rows on TOPS against the fp16 tensor peak"}
+            "note": "decode rows are measured in GB/s against HBM, prefill rows in TOPS against the fp16 tensor peak"}
 
 
 def run_decoder_layers(w4, wl, dev, stream, hbm, peak_src, steps=20, name="decoder_layers_m1_26x7"):
