@@ -85,3 +85,51 @@ def test_bad_arguments_rejected_before_launch(L):
     assert L.w4a8_debug_quantize_act(good, 1, 64, good, P(2), None) == 2
     # path argument
     assert L.w4a8_set_wait_budget(-1) == 1
+
+
+def test_new_entry_points_reject_bad_arguments(L):
+    """Shape and pointer checks of the gated pair, the RMS norm, the linear on
+    codes and decode attention return before any device work (no GPU here)."""
+    P = ctypes.c_void_p
+    good = P(4096)
+    fz = ctypes.c_size_t(0)
+    # gated pair
+    assert L.w4a8_linear_gated(good, good, good, 0, 8, 64, good, 1, None, fz, None) == 1
+    assert L.w4a8_linear_gated(good, good, good, 1, 8, 40, good, 1, None, fz, None) == 1
+    assert L.w4a8_linear_gated(good, P(4097), good, 1, 8, 64, good, 1, None, fz, None) == 2
+    # RMS norm emitting codes
+    f = ctypes.c_float
+    assert L.w4a8_rmsnorm_quant(good, None, good, f(1e-6), 1, 40, None, None, good, good, None) == 1
+    assert L.w4a8_rmsnorm_quant(good, None, good, f(-1.0), 1, 64, None, None, good, good, None) == 1
+    assert L.w4a8_rmsnorm_quant(good, None, good, f(float("nan")), 1, 64, None, None, good, good, None) == 1
+    assert L.w4a8_rmsnorm_quant(good, P(4098), good, f(1e-6), 1, 64, None, None, good, good, None) == 2
+    assert L.w4a8_rmsnorm_quant(good, None, good, f(1e-6), 1, 64, None, P(8), good, good, None) == 2
+    # linear on codes
+    assert L.w4a8_linear_q8(good, good, good, good, 1, 0, 64, good, None, fz, None) == 1
+    assert L.w4a8_linear_q8(P(4100), good, good, good, 1, 8, 64, good, None, fz, None) == 2
+    # decode attention: D, group size and head divisibility
+    assert L.w4a8_decode_attention(good, good, good, good, 1, 8, 1, 96, 64, good, None, fz, None) == 1
+    assert L.w4a8_decode_attention(good, good, good, good, 1, 6, 4, 64, 64, good, None, fz, None) == 1
+    assert L.w4a8_decode_attention(good, good, good, good, 1, 32, 1, 64, 64, good, None, fz, None) == 1
+    assert L.w4a8_decode_attention(good, good, good, good, 1, 8, 1, 64, 0, good, None, fz, None) == 1
+    assert L.w4a8_decode_attention(good, P(12), good, good, 1, 8, 1, 64, 64, good, None, fz, None) == 2
+
+
+def test_new_workspace_sizes(L):
+    """Workspace queries are pure host arithmetic: the fused decode routes
+    need none; the unfused gated route holds the 2N-row intermediate; the
+    attention combine needs space only beyond one 128-token chunk."""
+    L.w4a8_gated_workspace_bytes.restype = ctypes.c_size_t
+    L.w4a8_linear_q8_workspace_bytes.restype = ctypes.c_size_t
+    L.w4a8_decode_attention_workspace_bytes.restype = ctypes.c_size_t
+    assert L.w4a8_gated_workspace_bytes(1, 8192, 2048) == 0
+    assert L.w4a8_gated_workspace_bytes(64, 128, 256) >= 64 * 256 * 2
+    assert L.w4a8_linear_q8_workspace_bytes(1, 8192, 2048) == 0
+    assert L.w4a8_linear_q8_workspace_bytes(64, 128, 256) == L.w4a8_workspace_bytes(64, 128, 256, 2)
+    assert L.w4a8_decode_attention_workspace_bytes(4, 8, 1, 256, 128) == 0
+    nb = L.w4a8_decode_attention_workspace_bytes(4, 8, 1, 256, 129)
+    assert nb >= 4 * 8 * 2 * 256 * 4 + 4 * 8 * 2 * 2 * 4
+    assert L.w4a8_decode_attention_workspace_bytes(4, 8, 3, 256, 129) == 0      # invalid: 8 % 3
+    assert L.w4a8_prefill_splits(512, 8192, 2048) == 1
+    assert L.w4a8_prefill_splits(16, 128, 1024) == 8
+    assert L.w4a8_prefill_splits(0, 128, 1024) == 0
