@@ -282,7 +282,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
         const int rows = min(a.cr, nrows - c * a.cr);
         // RG consecutive rows per warp at a time: their shuffle reductions
         // are independent and overlap
-        for (int rb = warp * rgr; rb < rows; rb += CWARPS * rgr) {
+        for (int base = 0; base < rows;) {
+            // rows per warp in this pass: at most rgr, and no more than the
+            // remaining rows need, so the last pass spreads over all warps
+            const int rgp = min(rgr, (rows - base + CWARPS - 1) / CWARPS);
+            const int rb = base + warp * rgp;
+            base += CWARPS * rgp;
+            if (rb >= rows) continue;
             float v[RG * NV][MT];      // [output row g][branch] flattened
 #pragma unroll
             for (int g = 0; g < RG * NV; ++g)
@@ -316,7 +322,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
             for (int gv = 0; gv < RG * NV; ++gv) {
                 const int g = gv / NV, br = gv % NV;   // output row, branch (0 gate / plain, 1 up)
                 const int rr = rb + g;
-                if (g >= rgr || rr >= rows) break;
+                if (g >= rgp || rr >= rows) break;
                 const int n = r0 + c * a.cr + rr;
                 const uint8_t *wrow = wst + (size_t)br * w_stage + (size_t)rr * row_bytes;
                 const uint16_t *srow = sst + (size_t)br * a.cr * a.nb + (size_t)rr * a.nb;
@@ -373,7 +379,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
                 for (int m = 0; m < MT; ++m)
                     if (lane == g * MT + m) mine = GATED ? gate_act(a.act, v[g * NV][m]) * v[g * NV + NV - 1][m] : v[g][m];
             const int g = lane / MT, m = lane - (lane / MT) * MT;
-            if (lane < rgr * MT && rb + g < rows && m < a.M)
+            if (lane < rgp * MT && rb + g < rows && m < a.M)
                 a.out[(size_t)m * a.N + r0 + c * a.cr + rb + g] = __half_as_ushort(__float2half_rn(mine));
         }
         if (reuse) {
