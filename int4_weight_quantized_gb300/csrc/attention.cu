@@ -312,16 +312,10 @@ __global__ void attn_combine_kernel(const float *__restrict__ ws_o, const float 
 template <int D, int GP>
 w4a8_status launch_chunks(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *lens, int B, int Hq,
                           int Hkv, int Lmax, int nsplit, uint16_t *out, float *ws_o, float *ws_ml, cudaStream_t stream) {
-    static int attr_done[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W4A8_ERR_CUDA;
+    static std::atomic<int> attr_done[w4a8_host::kDeviceSlots];
     const size_t smem = attn_smem(D, GP);
-    if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(attn_chunk_kernel<D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return W4A8_ERR_CUDA;
-        attr_done[dev] = 1;
-    }
+    const w4a8_status ast = w4a8_host::ensure_smem_limit(attn_chunk_kernel<D, GP>, (int)smem, attr_done);
+    if (ast != W4A8_OK) return ast;
     int *status = w4a8_host::device_status_ptr();
     if (!status) return W4A8_ERR_CUDA;
     dim3 grid((unsigned)nsplit, (unsigned)Hkv, (unsigned)B);

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "w4a8.h"
 
 namespace w4a8 {
@@ -122,6 +124,28 @@ inline bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<
 inline w4a8_status launch_status() {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? W4A8_OK : W4A8_ERR_CUDA;
+}
+
+constexpr int kDeviceSlots = 64;   // devices a per-device table can hold
+
+// Raises a kernel's opt-in dynamic shared-memory limit on the current device
+// the first time it is launched there.  `done` is the kernel's own table of
+// per-device flags; it is atomic, so first calls from several host threads
+// at once are safe (each may set the attribute, which is idempotent).
+template <class Kernel>
+inline w4a8_status ensure_smem_limit(Kernel kern, int bytes, std::atomic<int> (&done)[kDeviceSlots]) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDeviceSlots) {
+        cudaGetLastError();
+        return W4A8_ERR_CUDA;
+    }
+    if (done[dev].load(std::memory_order_acquire)) return W4A8_OK;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A8_ERR_CUDA;
+    }
+    done[dev].store(1, std::memory_order_release);
+    return W4A8_OK;
 }
 
 }  // namespace w4a8_host

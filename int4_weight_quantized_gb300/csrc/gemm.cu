@@ -529,15 +529,9 @@ int pick_splits(int tiles, int nb) {
 template <bool DEBUG>
 w4a8_status launch_t(const CUtensorMap &ta, const CUtensorMap &tw, const CUtensorMap &ts, const GemmArgs &a,
                      dim3 grid, cudaStream_t stream) {
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(gemm_w4a8_tc_kernel<DEBUG>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess)
-            return W4A8_ERR_CUDA;
-        attr_set[dev] = true;
-    }
+    static std::atomic<int> attr_done[w4a8_host::kDeviceSlots];
+    const w4a8_status ast = w4a8_host::ensure_smem_limit(gemm_w4a8_tc_kernel<DEBUG>, SMEM_BYTES, attr_done);
+    if (ast != W4A8_OK) return ast;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(THREADS, 1, 1);

@@ -274,10 +274,11 @@ Plan make_plan(int M, int N, int K) {
 template <int MT, int G, bool DEBUG>
 w4a8_status launch_t(const Plan &p, const GemvArgs &a, cudaStream_t stream) {
     auto kern = gemv_kernel<MT, G, DEBUG>;
-    if (p.smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem) != cudaSuccess)
-            return W4A8_ERR_CUDA;
-    }
+    // the opt-in limit is raised once per device to the most any plan asks
+    // for, so concurrent calls with different plans never lower it
+    static std::atomic<int> attr_done[w4a8_host::kDeviceSlots];
+    const w4a8_status ast = w4a8_host::ensure_smem_limit(kern, 227 * 1024, attr_done);
+    if (ast != W4A8_OK) return ast;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = p.grid;
     cfg.blockDim = dim3(kThreads, 1, 1);

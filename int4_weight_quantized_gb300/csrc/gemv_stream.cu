@@ -455,14 +455,9 @@ Plan make_plan(int M, int N, int K, int nv = 1) {
 template <int MT, int BPL, bool DEBUG, bool GATED, bool Q8>
 w4a8_status launch_t(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
     auto kern = gemv_stream_kernel<MT, BPL, DEBUG, GATED, Q8>;
-    static int attr_done[64] = {};   // per device: the opt-in shared-memory limit is set once
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W4A8_ERR_CUDA;
-    if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALONE) != cudaSuccess)
-            return W4A8_ERR_CUDA;
-        attr_done[dev] = 1;
-    }
+    static std::atomic<int> attr_done[w4a8_host::kDeviceSlots];
+    const w4a8_status ast = w4a8_host::ensure_smem_limit(kern, SMEM_ALONE, attr_done);
+    if (ast != W4A8_OK) return ast;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
