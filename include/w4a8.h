@@ -62,7 +62,10 @@ typedef enum {
 typedef enum {
     W4A8_PATH_AUTO = 0,     /* w4a8_select_path decides */
     W4A8_PATH_DECODE = 1,   /* memory-bound GEMV, activations quantised in the kernel; M <= 8 per launch */
-    W4A8_PATH_PREFILL = 2   /* compute-bound tensor-core GEMM (tcgen05) after a quantisation pass */
+    W4A8_PATH_PREFILL = 2,  /* compute-bound tensor-core GEMM (tcgen05) after a quantisation pass */
+    W4A8_PATH_MID = 3       /* short sequences, M <= 64, K % 256 == 0: tensor-core kernel with the weights
+                               as the 128-row operand and the tokens (padded to 16, 32 or 64) as its N,
+                               streaming the weights once, after a quantisation pass */
 } w4a8_path;
 
 /* Activation of the gated pair's gate branch (w4a8_linear_gated). */
@@ -93,10 +96,17 @@ size_t w4a8_packed_bytes(int N, int K);
 w4a8_status w4a8_pack(const int8_t *w_codes, int N, int K, void *packed_w,
                       cudaStream_t stream);
 
-/* The kernel w4a8_linear would run for this shape (W4A8_PATH_DECODE or
- * W4A8_PATH_PREFILL): decode for M <= 8, prefill above.  Returns
- * W4A8_PATH_AUTO (0) for an invalid shape. */
+/* The kernel w4a8_linear would run for this shape: W4A8_PATH_DECODE for one
+ * or two tokens, W4A8_PATH_MID for 3 to 64 tokens (when K % 256 == 0; else
+ * decode up to 8 tokens), W4A8_PATH_PREFILL above.  Returns W4A8_PATH_AUTO
+ * (0) for an invalid shape. */
 int w4a8_select_path(int M, int N, int K);
+
+/* Number of CTAs along K per 128-row tile that W4A8_PATH_MID uses for this
+ * shape (1, 2, 4 or 8; a cluster whose fp32 partial tiles are summed in a
+ * fixed order through distributed shared memory).  0 when the mid path does
+ * not take the shape.  Informational. */
+int w4a8_mid_splits(int M, int N, int K);
 
 /* Number of CTAs along K per 128 x 128 output tile that the prefill path
  * uses for this shape: 1, 2, 4 or 8 (a thread-block cluster whose CTAs each
@@ -109,7 +119,7 @@ int w4a8_prefill_splits(int M, int N, int K);
 
 /* Device workspace in bytes that w4a8_linear_ex needs for this shape and
  * path (W4A8_PATH_AUTO resolves as w4a8_select_path); 0 when none.  The
- * prefill path keeps the quantised activations there. */
+ * prefill and mid paths keep the quantised activations there. */
 size_t w4a8_workspace_bytes(int M, int N, int K, int path);
 
 /* y = W4A8 linear of x.
@@ -119,9 +129,13 @@ size_t w4a8_workspace_bytes(int M, int N, int K, int path);
  *   out     [M][N] fp16, device; must not overlap the inputs.
  * Requires M >= 1, N >= 1, K >= 32, K % 32 == 0, and x finite (results are
  * unspecified otherwise).  Asynchronous on `stream`.  When the shape takes
- * the prefill path this call obtains its workspace with cudaMallocAsync on
- * `stream` and releases it with cudaFreeAsync after the kernels, so it is
- * stream-ordered; callers that must not allocate use w4a8_linear_ex. */
+ * the prefill or mid path this call obtains its workspace with
+ * cudaMallocAsync on `stream` and releases it with cudaFreeAsync after the
+ * kernels, so it is stream-ordered; callers that must not allocate use
+ * w4a8_linear_ex.  The tensor-core paths read packed_w and scales before
+ * they wait for the previous kernel on the stream (programmatic dependent
+ * launch): the weights must not be written by a kernel still running on
+ * the stream. */
 w4a8_status w4a8_linear(const uint16_t *x, const void *packed_w, const uint16_t *scales,
                         int M, int N, int K, uint16_t *out, cudaStream_t stream);
 

@@ -20,6 +20,7 @@ ACT_GELU_TANH = 2
 PATH_AUTO = 0
 PATH_DECODE = 1
 PATH_PREFILL = 2
+PATH_MID = 3
 
 STATUS = {0: "W4A8_OK", 1: "W4A8_ERR_INVALID_VALUE", 2: "W4A8_ERR_MISALIGNED", 3: "W4A8_ERR_CODE_RANGE",
           4: "W4A8_ERR_CUDA", 5: "W4A8_ERR_TIMEOUT", 6: "W4A8_ERR_UNSUPPORTED", 7: "W4A8_ERR_WORKSPACE"}
@@ -53,6 +54,8 @@ def lib():
         L.w4a8_select_path.restype = i
         L.w4a8_prefill_splits.argtypes = [i, i, i]
         L.w4a8_prefill_splits.restype = i
+        L.w4a8_mid_splits.argtypes = [i, i, i]
+        L.w4a8_mid_splits.restype = i
         L.w4a8_gated_workspace_bytes.argtypes = [i, i, i]
         L.w4a8_gated_workspace_bytes.restype = sz
         L.w4a8_linear_gated.argtypes = [P, P, P, i, i, i, P, i, P, sz, P]
@@ -117,6 +120,11 @@ def select_path(M, N, K):
 def prefill_splits(M, N, K):
     """CTAs along K per output tile that the prefill path uses (1, 2, 4 or 8)."""
     return lib().w4a8_prefill_splits(M, N, K)
+
+
+def mid_splits(M, N, K):
+    """CTAs along K per 128-row tile that the mid path uses (0 if it does not take the shape)."""
+    return lib().w4a8_mid_splits(M, N, K)
 
 
 def workspace_bytes(M, N, K, path=PATH_AUTO):

@@ -122,8 +122,16 @@ size_t w4a8_packed_bytes(int N, int K) {
 
 int w4a8_select_path(int M, int N, int K) {
     if (!shape_ok(M, N, K)) return W4A8_PATH_AUTO;
-    if (M <= 8 && (gemv_stream_supported(M, N, K) || gemv_supported(M, N, K))) return W4A8_PATH_DECODE;
+    const bool decode_ok = M <= 8 && (gemv_stream_supported(M, N, K) || gemv_supported(M, N, K));
+    if (M <= 2 && decode_ok) return W4A8_PATH_DECODE;
+    if (M <= 64 && mid_supported(M, N, K)) return W4A8_PATH_MID;
+    if (decode_ok) return W4A8_PATH_DECODE;
     return W4A8_PATH_PREFILL;
+}
+
+int w4a8_mid_splits(int M, int N, int K) {
+    if (!shape_ok(M, N, K) || !mid_supported(M, N, K)) return 0;
+    return tc_splits(M, N, K);
 }
 
 int w4a8_prefill_splits(int M, int N, int K) {
@@ -135,6 +143,7 @@ size_t w4a8_workspace_bytes(int M, int N, int K, int path) {
     if (!shape_ok(M, N, K)) return 0;
     if (path == W4A8_PATH_AUTO) path = w4a8_select_path(M, N, K);
     if (path == W4A8_PATH_PREFILL) return prefill_workspace_bytes(M, N, K);
+    if (path == W4A8_PATH_MID) return mid_supported(M, N, K) ? tc_workspace_bytes(M, N, K) : 0;
     return 0;
 }
 
@@ -162,6 +171,12 @@ static w4a8_status run_linear(const uint16_t *x, const void *packed_w, const uin
         size_t need = prefill_workspace_bytes(M, N, K);
         if (need && (workspace_bytes < need || !aligned16(workspace))) return W4A8_ERR_WORKSPACE;
         return launch_prefill(x, packed_w, scales, M, N, K, out, dots, workspace, stream);
+    }
+    if (path == W4A8_PATH_MID) {
+        if (!mid_supported(M, N, K)) return W4A8_ERR_UNSUPPORTED;
+        size_t need = tc_workspace_bytes(M, N, K);
+        if (workspace_bytes < need || !aligned16(workspace)) return W4A8_ERR_WORKSPACE;
+        return launch_tc_linear(x, packed_w, scales, M, N, K, out, dots, workspace, stream);
     }
     return W4A8_ERR_INVALID_VALUE;
 }
@@ -192,7 +207,7 @@ w4a8_status w4a8_linear_ex(const uint16_t *x, const void *packed_w, const uint16
                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     w4a8_status st = check_linear_args(x, packed_w, scales, M, N, K, out);
     if (st != W4A8_OK) return st;
-    if (path < W4A8_PATH_AUTO || path > W4A8_PATH_PREFILL) return W4A8_ERR_INVALID_VALUE;
+    if (path < W4A8_PATH_AUTO || path > W4A8_PATH_MID) return W4A8_ERR_INVALID_VALUE;
     return run_linear(x, packed_w, scales, M, N, K, out, nullptr, path, workspace, workspace_bytes, stream);
 }
 
@@ -274,7 +289,7 @@ w4a8_status w4a8_debug_block_dots(const uint16_t *x, const void *packed_w, const
     w4a8_status st = check_linear_args(x, packed_w, scales, M, N, K, out);
     if (st != W4A8_OK) return st;
     if (!aligned16(dots)) return W4A8_ERR_MISALIGNED;
-    if (path < W4A8_PATH_AUTO || path > W4A8_PATH_PREFILL) return W4A8_ERR_INVALID_VALUE;
+    if (path < W4A8_PATH_AUTO || path > W4A8_PATH_MID) return W4A8_ERR_INVALID_VALUE;
     return run_linear(x, packed_w, scales, M, N, K, out, dots, path, workspace, workspace_bytes, stream);
 }
 

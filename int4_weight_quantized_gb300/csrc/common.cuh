@@ -66,9 +66,29 @@ struct Quant8 {
     int sum;       // sum of the block's 32 codes (same in all 4 lanes)
 };
 
+// Reciprocal of the block scale used by the quantiser's fast path:
+// fl(127 / amax), with amax 0 mapped to 0 (every x of such a block is 0).
+__device__ __forceinline__ float act_recip(float amax) { return amax == 0.0f ? 0.0f : __fdiv_rn(127.0f, amax); }
+
+// Codes of one element by the definition, rint(fl(x / s)) clamped: the
+// fallback of the fast path below.
+static __device__ __noinline__ int act_code_exact(float x, float s) { return act_code(x, s); }
+
 // Quantise one block held by 4 consecutive lanes (lane % 4 == t), 8 fp16
 // values each.  Every lane of the warp must call this together (full-mask
 // shuffles of width 4); lanes with no data pass zeros.
+//
+// The codes equal rint(fl(x / s)) clamped to [-127, 127], s = fl(amax / 127),
+// but only the block's two scale divisions are IEEE divisions.  With
+// r = fl(127 / amax) and t = fl(x * r), the three roundings (of s, r and t)
+// each add a relative error of at most 2^-24, so for |x| <= amax
+//   |t - x/s| <= 127 * 3.0001 * 2^-24 < 2.28e-5,
+// and |fl(x/s) - x/s| <= 127 * 2^-24 < 7.6e-6, hence |t - fl(x/s)| < 2^-15.
+// When t is at least 2^-14 away from every half-integer, no rounding
+// boundary lies between t and fl(x/s), so rint(t) = rint(fl(x/s)); the
+// elements closer than that to a boundary (one in several thousand for
+// random data, and every exact tie) are divided exactly instead.  In both
+// cases |code| <= 127, so the clamp never changes a value.
 __device__ __forceinline__ Quant8 quant8_group4(uint4 xv) {
     const __half2 *h = reinterpret_cast<const __half2 *>(&xv);
     float f[8];
@@ -85,11 +105,28 @@ __device__ __forceinline__ Quant8 quant8_group4(uint4 xv) {
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2, 4));
     Quant8 r;
     r.s = act_scale(a);
+    const float rc = act_recip(a);
+    bool near = false;
+    float c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float t = f[i] * rc;
+        c[i] = rintf(t);
+        near |= fabsf(t - c[i]) > 0.5f - 0x1p-14f;
+    }
     int sum = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        r.q[i] = act_code(f[i], r.s);
+        r.q[i] = (int)c[i];
         sum += r.q[i];
+    }
+    if (near) {
+        sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            r.q[i] = act_code_exact(f[i], r.s);
+            sum += r.q[i];
+        }
     }
     sum += __shfl_xor_sync(0xffffffffu, sum, 1, 4);
     sum += __shfl_xor_sync(0xffffffffu, sum, 2, 4);

@@ -35,14 +35,10 @@
 // Every mbarrier wait is bounded (sync.cuh): on timeout the kernel records
 // W4A8_ERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies
 // and MMAs in flight, frees its tensor memory and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "common.cuh"
 #include "kernels.h"
 #include "sync.cuh"
+#include "tc.cuh"
 
 namespace {
 
@@ -58,7 +54,6 @@ constexpr int NP = 2;              // accumulator pairs in TMEM (2 x 2 x 128 col
 constexpr int TILE = 128 * 128;    // bytes of one 128-row x 64-k fp16 tile (one 128-byte-swizzle atom column)
 constexpr int W_BYTES = BM * KS / 2;        // 4 KB, packed int4 of one stage
 constexpr int SX_BYTES = SXG * BN * 4;      // 4 KB, SXG blocks of s_x
-constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;          // 2 per TMEM lane quarter, 64 token columns each
 constexpr int CONV_WARP0 = 3;        // warps 3..6 convert weights (32 rows each)
 constexpr int EPI_WARP0 = 7;         // warps 7..14 run the epilogue
@@ -85,64 +80,8 @@ struct GemmArgs {
     int bps;                 // 32-blocks per split (even)
 };
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-                 ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T, fp16 inputs, fp32 accumulate.
-__device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
-}
-
-// Makes this thread's generic-proxy shared-memory writes visible to the
-// async proxy (the tensor cores read operand tiles through it).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major rows of 128 bytes, 128-byte
-// swizzle, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;                  // leading byte offset (unused with this swizzle)
-    d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset
-    d |= (uint64_t)1 << 46;                  // descriptor version
-    d |= (uint64_t)2 << 61;                  // 128-byte swizzle
-    return d;
-}
-
 // Instruction descriptor: fp32 accumulator, fp16 A and B, both K-major.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-
-#define TC_LD32(taddr, r)                                                                                     \
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15," \
-                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                   \
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),         \
-                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),     \
-                   "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),  \
-                   "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),  \
-                   "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])                                          \
-                 : "r"(taddr))
-
-// Two int4 weights (nibbles i and i+4 of a packed word, stored as w+8) to an
-// exact fp16 pair: 0x6400 | u is the fp16 value 1024 + u; subtracting 1032
-// leaves u - 8 = w.
-__device__ __forceinline__ uint32_t nibbles_to_half2(uint32_t word_shifted) {
-    uint32_t t = (word_shifted & 0x000F000Fu) | 0x64006400u;
-    __half2 h = __hsub2(*reinterpret_cast<__half2 *>(&t), __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
-    return *reinterpret_cast<uint32_t *>(&h);
-}
 
 // Bounded wait by every lane of a warp, with one warp-wide outcome (the
 // tcgen05.ld/st that follow are warp-collective).  A failed wait raises the
@@ -152,28 +91,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
     ok = __all_sync(0xffffffffu, ok);
     if (!ok && (threadIdx.x & 31) == 0) *abort_flag = 1u;
     return ok;
-}
-
-// All threads of all CTAs of the cluster; release/acquire orders the shared
-// memory writes before it with the reads after it, cluster-wide.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// Address of the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local_addr, uint32_t rank) {
-    uint32_t ra;
-    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
-    return ra;
-}
-
-// fp32 load from distributed shared memory.  Volatile, so it stays after the
-// cluster barrier, but without a memory clobber; callers issue a batch of
-// these before using any of the results.
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
 }
 
 // Sum of the S partial tiles for W/2 columns of one row, in split order.
@@ -248,11 +165,7 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
         misc[1] = 0;
         fence_barrier_init();
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32((const void *)&misc[0])), "r"(TMEM_COLS) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 1) tmem_alloc_512(smem_u32((const void *)&misc[0]));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -318,7 +231,7 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
                         const uint32_t off = (uint32_t)(j * 64 + kk * 32);
-                        tc_mma_ss(tmem + (uint32_t)((2 * pr + j) * BN), smem_desc_sw128(abase + off),
+                        tc_mma_f16(tmem + (uint32_t)((2 * pr + j) * BN), smem_desc_sw128(abase + off),
                                   smem_desc_sw128(bbase + off), kIdesc, (uint32_t)kk);
                     }
                 }
@@ -344,14 +257,7 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
             const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
             uint8_t *row = smem + OFF_A + slot * TILE + r * 128;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 v;
-                v.x = nibbles_to_half2(wd[c]);
-                v.y = nibbles_to_half2(wd[c] >> 4);
-                v.z = nibbles_to_half2(wd[c] >> 8);
-                v.w = nibbles_to_half2(wd[c] >> 12);
-                *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = v;
-            }
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = int4x8_to_half8(wd[c]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&conv[slot]);
@@ -401,8 +307,8 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t d[32];
-                    TC_LD32(tbase + (uint32_t)((2 * pr + j) * BN + h * 32), d);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    tmem_ld_cols<32>(tbase + (uint32_t)((2 * pr + j) * BN + h * 32), d);
+                    tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
                         const float4 sx4 = *reinterpret_cast<const float4 *>(sxp + h * 32 + i);
@@ -451,7 +357,7 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
         // Split-K: the CTAs of the cluster hold the partial tiles of their K
         // ranges; CTA z sums columns [z*W, (z+1)*W) of all of them through
         // distributed shared memory, in split order (fixed, deterministic).
-        cluster_sync();
+        cluster_sync_all();
         if (warp >= EPI_WARP0) {
             const int t = threadIdx.x - EPI_WARP0 * 32;
             const uint32_t red = sbase + OFF_ACT;
@@ -460,46 +366,18 @@ gemm_w4a8_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_con
             else if (a.splits == 4) reduce_splits<4>(red, blockIdx.z, t, n0, m0, a, ok);
             else reduce_splits<8>(red, blockIdx.z, t, n0, m0, a, ok);
         }
-        cluster_sync();   // no CTA leaves while a peer may still read its tile
+        cluster_sync_all();   // no CTA leaves while a peer may still read its tile
     }
 
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+        tmem_dealloc_512(tmem);
     }
 }
 
 // ------------------------------------------------------------------ host side
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void *p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
-bool make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *base, uint64_t inner, uint64_t outer,
-                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * (cuuint64_t)esize};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
 
 int m_pad(int M) { return (M + BN - 1) / BN * BN; }
 
@@ -555,19 +433,25 @@ w4a8_status launch_t(const CUtensorMap &ta, const CUtensorMap &tw, const CUtenso
 
 namespace w4a8_host {
 
+// Shapes with K % 256 == 0 run on the tensor-core kernel of gemm_mid.cu
+// (128-token tiles); this file's kernel takes the others.
+
 int prefill_splits(int M, int N, int K) {
+    if (tc_supported(M, N, K)) return tc_splits(M, N, K);
     return pick_splits(((N + BM - 1) / BM) * (m_pad(M) / BN), K / 32);
 }
 
+int prefill_tokens_padded(int M, int N, int K) { return tc_supported(M, N, K) ? tc_tokens_padded(M) : m_pad(M); }
+
 size_t prefill_workspace_bytes(int M, int N, int K) {
-    (void)N;
-    const size_t mp = (size_t)m_pad(M);
+    const size_t mp = (size_t)prefill_tokens_padded(M, N, K);
     return mp * (size_t)K * 2 + (size_t)(K / 32) * mp * 4;
 }
 
 w4a8_status launch_prefill(const uint16_t *x, const void *packed_w, const uint16_t *scales,
                            int M, int N, int K, uint16_t *out, int32_t *dots, void *workspace,
                            cudaStream_t stream) {
+    if (tc_supported(M, N, K)) return launch_tc_linear(x, packed_w, scales, M, N, K, out, dots, workspace, stream);
     const int mp = m_pad(M);
     uint16_t *q16 = static_cast<uint16_t *>(workspace);
     float *sx = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + (size_t)mp * K * 2);
@@ -578,14 +462,15 @@ w4a8_status launch_prefill(const uint16_t *x, const void *packed_w, const uint16
 
 w4a8_status launch_prefill_gemm(const uint16_t *q16, const float *sx, const void *packed_w, const uint16_t *scales,
                                 int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream) {
+    if (tc_supported(M, N, K)) return launch_tc_gemm(q16, sx, packed_w, scales, M, N, K, out, dots, stream);
     const int mp = m_pad(M);
     const int nb = K / 32;
     CUtensorMap ta, tw, ts;
-    if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, q16, (uint64_t)K, (uint64_t)mp, 64, BN,
+    if (!w4a8_host::make_tensor_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, q16, (uint64_t)K, (uint64_t)mp, 64, BN,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, packed_w, (uint64_t)K / 2, (uint64_t)N, KS / 2, BM,
+        !w4a8_host::make_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, packed_w, (uint64_t)K / 2, (uint64_t)N, KS / 2, BM,
                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sx, (uint64_t)mp, (uint64_t)nb, BN, SXG,
+        !w4a8_host::make_tensor_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sx, (uint64_t)mp, (uint64_t)nb, BN, SXG,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4A8_ERR_CUDA;
 

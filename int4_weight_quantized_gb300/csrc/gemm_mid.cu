@@ -1,0 +1,572 @@
+// gemm_mid.cu -- W4A8 linear for short sequences (3 to 64 tokens) on the
+// 5th-generation tensor cores, with the weights as the 128-row operand.
+//
+// Stage-aware kernel choice ("Що змінює ML Drift для on-device
+// AI-інференсу на вашому телефоні?", tech.dede.sh, section "Stage-aware
+// оптимізація для великих мовних моделей"; "谷歌突然开源！端侧 AI 的 GPU
+// 底座，要变了", m.x-techcon.com, section "对大模型，重点已经从“算得快”变成
+// “数据少搬”"): between one-token decode (a memory-bound GEMV) and long
+// prefill (a compute-bound GEMM) lies a range of token counts where the
+// weight stream still sets the time but dp4a per token costs too many
+// instructions.  Here the tokens are the MMA's N dimension (padded to 16, 32
+// or 64) and every CTA streams 128 weight rows through a deep ring, so the
+// tensor cores do the block dots and the weights are read once.
+//
+// Per CTA (128 weight rows, a range of K, all tokens):
+//   - warp 0 streams the packed int4 weight tiles (128 rows x 64 k = 4 KB)
+//     by TMA into a 16-deep ring; it starts before the kernel waits for the
+//     quantisation pass (programmatic dependent launch);
+//   - warps 4-7 expand them into fp16 (exact: -8..7) in the 128-byte-swizzled
+//     K-major layout of the MMA's A operand;
+//   - warp 3 loads the activation codes (fp16, written by the quantisation
+//     pass) as the B operand, warp 2 the block scales s_w and s_x;
+//   - warp 1 issues tcgen05.mma (M = 128 rows, N = tokens, K = 16), two per
+//     32-block, each block into its own TMEM accumulator of N columns; four
+//     accumulator units of 128 columns cycle between it and the epilogue;
+//   - warps 8-15 read each block's exact integer dots (tcgen05.ld) and apply
+//     acc += d * (s_w * s_x) in fp32 (pairs of tokens per instruction);
+//   - with several CTAs along K (a thread-block cluster), the fp32 partial
+//     tiles are summed in a fixed order through distributed shared memory.
+//
+// Every mbarrier wait is bounded (sync.cuh): on timeout the kernel records
+// W4A8_ERR_TIMEOUT, stops issuing, waits (bounded) for its own copies and
+// MMAs, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sync.cuh"
+#include "tc.cuh"
+
+namespace {
+
+using namespace w4a8;
+
+constexpr int BM = 128;           // weight rows per CTA: MMA M, TMEM lanes
+constexpr int KS = 64;            // k per stage: two 32-blocks
+constexpr int AS = 4;             // fp16 weight (A operand) stages
+constexpr int XS = 4;             // activation (B operand) stages
+constexpr int SG = 16;            // 32-blocks per scale load
+constexpr int SS = 3;             // scale stages
+constexpr int UNITS = 4;          // TMEM accumulator units of 128 columns (all 512)
+constexpr int A_TILE = BM * KS * 2;            // 16 KB
+constexpr int W_TILE = BM * KS / 2;            // 4 KB
+constexpr int SW_TILE = BM * SG * 2;           // 4 KB
+constexpr int CONV_WARP0 = 4;
+constexpr int EPI_WARP0 = 8;
+constexpr int EPI_WARPS = 8;      // 2 per TMEM lane quarter, half of the tokens each
+constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
+
+template <int NT>
+struct Layout {
+    static constexpr int WS = NT == 128 ? 8 : 16;          // packed weight stages (4 KB each)
+    static constexpr int X_TILE = NT * KS * 2;            // NT tokens x 64 k fp16
+    static constexpr int SX_TILE = SG * NT * 4;            // 16 blocks x NT tokens fp32
+    static constexpr int UB = 128 / NT;                    // blocks per accumulator unit
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_X = OFF_A + AS * A_TILE;
+    static constexpr int OFF_W = OFF_X + XS * X_TILE;
+    static constexpr int OFF_SW = OFF_W + WS * W_TILE;
+    static constexpr int OFF_SX = OFF_SW + SS * SW_TILE;
+    static constexpr int OFF_BAR = OFF_SX + SS * SX_TILE;
+    // wfull, wempty; afull, aempty; xfull, xempty; sfull, sempty; accfull, accempty; final
+    static constexpr int NUM_BARS = 2 * WS + 2 * AS + 2 * XS + 2 * SS + 2 * UNITS + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM = OFF_MISC + 16 + 1024;     // + slack to align the base to 1024
+    static_assert(128 * NT * 4 <= AS * A_TILE, "split-K partial tile must fit the A ring");
+};
+
+struct MidArgs {
+    uint16_t *out;           // [M][N] fp16
+    int32_t *dots;           // debug: [M][N][nb]
+    int *status;
+    long long budget;
+    int M, N, nb;            // blockIdx.y is the tile of NT tokens
+    int splits;              // CTAs of a cluster along K; blockIdx.z is the split
+    int bps;                 // 32-blocks per split (multiple of 16)
+};
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Bounded wait by every lane of a warp, with one warp-wide outcome.  A failed
+// wait raises the CTA's abort flag; once it is up, waits fail at once.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const MidArgs &a,
+                                          volatile uint32_t *abort_flag) {
+    bool ok = (*abort_flag == 0u) && (mbar_test_wait(bar, parity) || mbar_wait_bounded(bar, parity, a.budget, a.status));
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && (threadIdx.x & 31) == 0) *abort_flag = 1u;
+    return ok;
+}
+
+// Single-thread bounded wait; raises the abort flag on failure.
+__device__ __forceinline__ bool one_wait(uint64_t *bar, uint32_t parity, const MidArgs &a, volatile uint32_t *abort_flag) {
+    if (*abort_flag) return false;
+    if (mbar_test_wait(bar, parity) || mbar_wait_bounded(bar, parity, a.budget, a.status)) return true;
+    *abort_flag = 1u;
+    return false;
+}
+
+// fp32 pair ops (two lanes of work per instruction; each result is the
+// correctly rounded fp32 operation, as with the scalar forms).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    unsigned long long r, x, y;
+    asm("mov.b64 %0, {%1,%2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1,%2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    float2 o;
+    asm("mov.b64 {%0,%1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    unsigned long long r, x, y, z;
+    asm("mov.b64 %0, {%1,%2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1,%2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1,%2};" : "=l"(z) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(y), "l"(z));
+    float2 o;
+    asm("mov.b64 {%0,%1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+
+// acc[token pairs] += d * (s_w * s_x) for CNT consecutive tokens of one
+// block (d: exact integer dots from TMEM as fp32 bit patterns; sxp: the
+// block's s_x of those tokens); the debug instantiation also stores each dot.
+template <int CNT, bool DEBUG>
+__device__ __forceinline__ void scale_acc(float2 *acc, const uint32_t *d, float sw, const float *sxp, int n, int mbase,
+                                          int b, const MidArgs &a) {
+    const float2 sw2 = make_float2(sw, sw);
+#pragma unroll
+    for (int i = 0; i < CNT; i += 4) {
+        const float4 s4 = *reinterpret_cast<const float4 *>(sxp + i);
+        const float2 p01 = mul2(sw2, make_float2(s4.x, s4.y));
+        const float2 p23 = mul2(sw2, make_float2(s4.z, s4.w));
+        const float2 d01 = make_float2(__uint_as_float(d[i]), __uint_as_float(d[i + 1]));
+        const float2 d23 = make_float2(__uint_as_float(d[i + 2]), __uint_as_float(d[i + 3]));
+        acc[i / 2] = fma2(d01, p01, acc[i / 2]);
+        acc[i / 2 + 1] = fma2(d23, p23, acc[i / 2 + 1]);
+        if (DEBUG && n < a.N) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int m = mbase + i + v;
+                if (m < a.M) a.dots[((size_t)m * a.N + n) * a.nb + b] = (int32_t)__uint_as_float(d[i + v]);
+            }
+        }
+    }
+}
+
+template <int NT, bool DEBUG>
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_sx, MidArgs a) {
+    using LY = Layout<NT>;
+    constexpr int WS = LY::WS;
+    constexpr int UB = LY::UB;
+    constexpr int HT = NT / 2;                 // tokens per epilogue thread
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + LY::OFF_BAR);
+    uint64_t *wfull = bars, *wempty = wfull + WS;
+    uint64_t *afull = wempty + WS, *aempty = afull + AS;
+    uint64_t *xfull = aempty + AS, *xempty = xfull + XS;
+    uint64_t *sfull = xempty + XS, *sempty = sfull + SS;
+    uint64_t *accfull = sempty + SS, *accempty = accfull + UNITS;
+    uint64_t *finalb = accempty + UNITS;
+    volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + LY::OFF_MISC);   // [0] tmem, [1] abort
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BM;
+    const int m0 = blockIdx.y * NT;
+    const int b0 = blockIdx.z * a.bps;
+    const int nbl = max(0, min(a.nb, b0 + a.bps) - b0);    // this CTA's 32-blocks (multiple of 8)
+    const int nst = nbl / 2;                                 // stages
+    const int nunits = nbl / UB;
+    const int ngroups = (nbl + SG - 1) / SG;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < WS; ++s) { mbar_init(&wfull[s], 1); mbar_init(&wempty[s], 4); }
+        for (int s = 0; s < AS; ++s) { mbar_init(&afull[s], 4); mbar_init(&aempty[s], 1); }
+        for (int s = 0; s < XS; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
+        for (int s = 0; s < SS; ++s) { mbar_init(&sfull[s], 1); mbar_init(&sempty[s], EPI_WARPS); }
+        for (int s = 0; s < UNITS; ++s) { mbar_init(&accfull[s], 1); mbar_init(&accempty[s], EPI_WARPS); }
+        mbar_init(finalb, 1);
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc_512(smem_u32((const void *)&misc[0]));
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- weights (TMA), before the dependency wait
+        if (lane == 0) {
+            int issued = 0;
+            for (int s = 0; s < nst; ++s) {
+                const int slot = s % WS;
+                if (!one_wait(&wempty[slot], ((uint32_t)(s / WS) & 1u) ^ 1u, a, misc + 1)) break;
+                mbar_arrive_expect_tx(&wfull[slot], W_TILE);
+                tma_load_2d(sbase + LY::OFF_W + slot * W_TILE, &tm_w, (b0 + 2 * s) * 16, n0, smem_u32(&wfull[slot]));
+                issued = s + 1;
+            }
+            for (int s = (issued > WS ? issued - WS : 0); s < issued; ++s)
+                mbar_wait_bounded(&wfull[s % WS], (uint32_t)(s / WS) & 1u, a.budget, nullptr);
+        }
+    } else if (warp == 2 || warp == 3) {
+        // ---------------------------------------------------------- scales (warp 2), activation codes (warp 3)
+        pdl_wait();
+        if (lane == 0) {
+            const bool sc = warp == 2;
+            const int S = sc ? SS : XS;
+            uint64_t *fb = sc ? sfull : xfull;
+            uint64_t *eb = sc ? sempty : xempty;
+            const int nloads = sc ? ngroups : nst;
+            int issued = 0;
+            for (int s = 0; s < nloads; ++s) {
+                const int slot = s % S;
+                if (!one_wait(&eb[slot], ((uint32_t)(s / S) & 1u) ^ 1u, a, misc + 1)) break;
+                if (sc) {
+                    mbar_arrive_expect_tx(&fb[slot], SW_TILE + LY::SX_TILE);
+                    tma_load_2d(sbase + LY::OFF_SW + slot * SW_TILE, &tm_sw, b0 + SG * s, n0, smem_u32(&fb[slot]));
+                    tma_load_2d(sbase + LY::OFF_SX + slot * LY::SX_TILE, &tm_sx, m0, b0 + SG * s, smem_u32(&fb[slot]));
+                } else {
+                    mbar_arrive_expect_tx(&fb[slot], LY::X_TILE);
+                    tma_load_2d(sbase + LY::OFF_X + slot * LY::X_TILE, &tm_x, (b0 + 2 * s) * 32, m0, smem_u32(&fb[slot]));
+                }
+                issued = s + 1;
+            }
+            for (int s = (issued > S ? issued - S : 0); s < issued; ++s)
+                mbar_wait_bounded(&fb[s % S], (uint32_t)(s / S) & 1u, a.budget, nullptr);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+            for (int s = 0; s < nst; ++s) {
+                const int as = s % AS, xs = s % XS;
+                if (!one_wait(&afull[as], (uint32_t)(s / AS) & 1u, a, misc + 1)) break;
+                if (!one_wait(&xfull[xs], (uint32_t)(s / XS) & 1u, a, misc + 1)) break;
+                bool ok = true;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int b = 2 * s + j, u = b / UB, jj = b - u * UB;
+                    if (jj == 0 && !one_wait(&accempty[u % UNITS], ((uint32_t)(u / UNITS) & 1u) ^ 1u, a, misc + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)((u % UNITS) * 128 + jj * NT);
+                    const uint32_t ab = sbase + LY::OFF_A + as * A_TILE + j * 64;
+                    const uint32_t xb = sbase + LY::OFF_X + xs * LY::X_TILE + j * 64;
+                    tc_mma_f16(d, smem_desc_sw128(ab), smem_desc_sw128(xb), idesc, 0u);
+                    tc_mma_f16(d, smem_desc_sw128(ab + 32), smem_desc_sw128(xb + 32), idesc, 1u);
+                    if (jj == UB - 1) tc_commit(smem_u32(&accfull[u % UNITS]));
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&aempty[as]));
+                tc_commit(smem_u32(&xempty[xs]));
+            }
+            // every MMA issued so far has completed once this barrier flips
+            tc_commit(smem_u32(finalb));
+            mbar_wait_bounded(finalb, 0, a.budget, nullptr);
+        }
+    } else if (warp >= CONV_WARP0 && warp < CONV_WARP0 + 4) {
+        // ---------------------------------------------------------- int4 -> fp16 A tiles
+        // Thread r expands its row's 64 weights of the stage into 8 chunks of
+        // 16 bytes, chunk c at position c ^ (r % 8) of the row's 128 bytes.
+        // The packed slot is released only after the values read from it
+        // have been used (the fp16 stores depend on them): a release right
+        // after issuing the loads could let the next TMA copy into the slot
+        // overtake them.
+        const int r = (warp - CONV_WARP0) * 32 + lane;
+        for (int s = 0; s < nst; ++s) {
+            const int ws = s % WS, as = s % AS;
+            if (!warp_wait(&wfull[ws], (uint32_t)(s / WS) & 1u, a, misc + 1)) break;
+            if (!warp_wait(&aempty[as], ((uint32_t)(s / AS) & 1u) ^ 1u, a, misc + 1)) break;
+            const uint4 *src = reinterpret_cast<const uint4 *>(smem + LY::OFF_W + ws * W_TILE + r * (KS / 2));
+            const uint4 p0 = src[0], p1 = src[1];
+            const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            uint8_t *row = smem + LY::OFF_A + as * A_TILE + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = int4x8_to_half8(wd[c]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&afull[as]);
+                mbar_arrive(&wempty[ws]);
+            }
+        }
+    } else if (warp >= EPI_WARP0) {
+        // ---------------------------------------------------------- epilogue
+        const int e = warp - EPI_WARP0;
+        const int q = warp & 3;                       // TMEM lane quarter this warp may access
+        const int t0 = (e >> 2) * HT;                 // this warp's first token
+        const int r = q * 32 + lane;
+        const int n = n0 + r;
+        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)t0;
+        float2 acc[HT / 2];
+#pragma unroll
+        for (int i = 0; i < HT / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
+        bool ok = true;
+        pdl_wait();                                   // outputs are written below
+        for (int u = 0; u < nunits && ok; ++u) {
+            const int bu = u * UB;                    // first local block of the unit
+            const int g = bu / SG;
+            if (bu % SG == 0 && !warp_wait(&sfull[g % SS], (uint32_t)(g / SS) & 1u, a, misc + 1)) {
+                ok = false;
+                break;
+            }
+            // this row's s_w of the unit's UB blocks (fp16 pairs), one vector load
+            uint32_t swu[UB > 1 ? UB / 2 : 1];
+            {
+                const uint8_t *sp = smem + LY::OFF_SW + (g % SS) * SW_TILE + r * (SG * 2) + (bu % SG) * 2;
+                if constexpr (UB == 8) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sp);
+                    swu[0] = v.x; swu[1] = v.y; swu[2] = v.z; swu[3] = v.w;
+                } else if constexpr (UB == 4) {
+                    const uint2 v = *reinterpret_cast<const uint2 *>(sp);
+                    swu[0] = v.x; swu[1] = v.y;
+                } else if constexpr (UB == 2) {
+                    swu[0] = *reinterpret_cast<const uint32_t *>(sp);
+                } else {
+                    swu[0] = *reinterpret_cast<const uint16_t *>(sp);
+                }
+            }
+            if (!warp_wait(&accfull[u % UNITS], (uint32_t)(u / UNITS) & 1u, a, misc + 1)) { ok = false; break; }
+            tc_fence_after();
+            const float *sxt = reinterpret_cast<const float *>(smem + LY::OFF_SX + (g % SS) * LY::SX_TILE);
+            const uint32_t tu = tbase + (uint32_t)((u % UNITS) * 128);
+            if constexpr (NT <= 64) {
+                // all UB blocks of the unit in one batch of loads (UB * HT = 64 columns)
+                uint32_t d[UB][HT];
+#pragma unroll
+                for (int j = 0; j < UB; ++j) tmem_ld_cols<HT>(tu + (uint32_t)(j * NT), d[j]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&accempty[u % UNITS]);
+#pragma unroll
+                for (int j = 0; j < UB; ++j) {
+                    const int bl = bu + j;
+                    const uint32_t pr = swu[j >> 1];
+                    const float sw = __half2float(__ushort_as_half((uint16_t)((j & 1) ? (pr >> 16) : (pr & 0xffffu))));
+                    scale_acc<HT, DEBUG>(acc, d[j], sw, sxt + (bl % SG) * NT + t0, n, m0 + t0, b0 + bl, a);
+                }
+            } else {
+                // one block of 128 tokens: this thread's 64 columns in two halves
+                const float sw = __half2float(__ushort_as_half((uint16_t)(swu[0] & 0xffffu)));
+                const float *sxp = sxt + (bu % SG) * NT + t0;
+                uint32_t d[32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    tmem_ld_cols<32>(tu + (uint32_t)(h * 32), d);
+                    tmem_ld_wait();
+                    if (h == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&accempty[u % UNITS]);
+                    }
+                    scale_acc<32, DEBUG>(acc + h * 16, d, sw, sxp + h * 32, n, m0 + t0 + h * 32, b0 + bu, a);
+                }
+            }
+            const int bl_last = bu + UB - 1;
+            if (bl_last % SG == SG - 1 || bl_last == nbl - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sempty[g % SS]);
+            }
+        }
+        if (a.splits > 1) {
+            // partial tile of this K range -> shared memory, [token][row]
+            // (the A ring is idle: every MMA has completed)
+            float *red = reinterpret_cast<float *>(smem + LY::OFF_A);
+#pragma unroll
+            for (int i = 0; i < HT / 2; ++i) {
+                red[(t0 + 2 * i) * BM + r] = acc[i].x;
+                red[(t0 + 2 * i + 1) * BM + r] = acc[i].y;
+            }
+        } else if (ok && misc[1] == 0u && n < a.N) {
+#pragma unroll
+            for (int i = 0; i < HT / 2; ++i) {
+                const int m = m0 + t0 + 2 * i;
+                if (m < a.M) a.out[(size_t)m * a.N + n] = __half_as_ushort(__float2half_rn(acc[i].x));
+                if (m + 1 < a.M) a.out[(size_t)(m + 1) * a.N + n] = __half_as_ushort(__float2half_rn(acc[i].y));
+            }
+        }
+    }
+
+    if (a.splits > 1) {
+        // CTA z sums tokens [z*NT/S, (z+1)*NT/S) of every peer's partial tile
+        // through distributed shared memory, in split order (deterministic).
+        cluster_sync_all();
+        if (warp >= EPI_WARP0) {
+            const int t = threadIdx.x - EPI_WARP0 * 32;
+            const uint32_t red = sbase + LY::OFF_A;
+            const int S = a.splits;
+            const int w = NT / S;                      // tokens reduced by this CTA
+            const int c0 = (int)blockIdx.z * w;
+            const bool okk = misc[1] == 0u;
+            for (int idx = t; idx < w * BM; idx += EPI_WARPS * 32) {
+                const int rr = idx % BM, c = c0 + idx / BM;
+                const uint32_t off = (uint32_t)((c * BM + rr) * 4);
+                float v[8];
+#pragma unroll
+                for (int z = 0; z < 8; ++z) v[z] = z < S ? ld_dsmem_f32(dsmem_addr(red + off, (uint32_t)z)) : 0.0f;
+                float sum = 0.0f;
+#pragma unroll
+                for (int z = 0; z < 8; ++z)
+                    if (z < S) sum += v[z];
+                const int nn = n0 + rr, m = m0 + c;
+                if (okk && nn < a.N && m < a.M) a.out[(size_t)m * a.N + nn] = __half_as_ushort(__float2half_rn(sum));
+            }
+        }
+        cluster_sync_all();   // no CTA leaves while a peer may still read its tile
+    }
+
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_512(tmem);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+constexpr int kSMs = 152;
+
+int nt_for(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
+
+// CTAs along K per 128-row tile: the tile count alone leaves SMs idle for
+// narrow layers, so K is split over S CTAs (S in 1..8, 16-block multiples)
+// minimising the waves of one-CTA-per-SM launches times the blocks per CTA,
+// plus a per-CTA fixed cost of about 24 blocks (pipeline fill, reduction).
+int pick_mid_splits(int tiles, int nb) {
+    int best = 1;
+    long best_cost = -1;
+    for (int S = 1; S <= 8; S *= 2) {
+        const int bps = SG * ((nb + SG * S - 1) / (SG * S));
+        if (S > 1 && (S - 1) * bps >= nb) break;          // a split would be empty
+        const long waves = ((long)tiles * S + kSMs - 1) / kSMs;
+        const long cost = waves * (bps + 24);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = S;
+        }
+    }
+    return best;
+}
+
+template <int NT, bool DEBUG>
+w4a8_status launch_nt(const CUtensorMap &tw, const CUtensorMap &tx, const CUtensorMap &tsw, const CUtensorMap &tsx,
+                      const MidArgs &a, dim3 grid, cudaStream_t stream) {
+    static std::atomic<int> attr_done[w4a8_host::kDeviceSlots];
+    const w4a8_status ast = w4a8_host::ensure_smem_limit(gemm_mid_kernel<NT, DEBUG>, Layout<NT>::SMEM, attr_done);
+    if (ast != W4A8_OK) return ast;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Layout<NT>::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (a.splits > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = (unsigned)a.splits;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    if (cudaLaunchKernelEx(&cfg, gemm_mid_kernel<NT, DEBUG>, tw, tx, tsw, tsx, a) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A8_ERR_CUDA;
+    }
+    return w4a8_host::launch_status();
+}
+
+}  // namespace
+
+namespace w4a8_host {
+
+bool tc_supported(int M, int N, int K) { return M >= 1 && N >= 1 && K >= 256 && K % 256 == 0; }
+
+bool mid_supported(int M, int N, int K) { return M <= 64 && tc_supported(M, N, K); }
+
+int tc_tokens_padded(int M) { return M <= 64 ? nt_for(M) : (M + 127) / 128 * 128; }
+
+int tc_splits(int M, int N, int K) {
+    const int mp = tc_tokens_padded(M);
+    const int nt = M <= 64 ? mp : 128;
+    return pick_mid_splits(((N + BM - 1) / BM) * (mp / nt), K / 32);
+}
+
+size_t tc_workspace_bytes(int M, int N, int K) {
+    (void)N;
+    const size_t mp = (size_t)tc_tokens_padded(M);
+    return mp * (size_t)K * 2 + (size_t)(K / 32) * mp * 4;
+}
+
+w4a8_status launch_tc_gemm(const uint16_t *q16, const float *sx, const void *packed_w, const uint16_t *scales, int M,
+                           int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream) {
+    if (!tc_supported(M, N, K)) return W4A8_ERR_UNSUPPORTED;
+    const int mp = tc_tokens_padded(M);
+    const int NT = M <= 64 ? mp : 128;
+    const int nb = K / 32;
+    CUtensorMap tw, tx, tsw, tsx;
+    if (!make_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, packed_w, (uint64_t)K / 2, (uint64_t)N, KS / 2, BM,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, q16, (uint64_t)K, (uint64_t)mp, KS, NT,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_2d(&tsw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, (uint64_t)nb, (uint64_t)N, SG, BM,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tensor_map_2d(&tsx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sx, (uint64_t)mp, (uint64_t)nb, NT, SG,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+        return W4A8_ERR_CUDA;
+
+    MidArgs a;
+    a.out = out;
+    a.dots = dots;
+    a.status = device_status_ptr();
+    a.budget = wait_budget();
+    a.M = M;
+    a.N = N;
+    a.nb = nb;
+    if (!a.status) return W4A8_ERR_CUDA;
+    a.splits = tc_splits(M, N, K);
+    a.bps = SG * ((nb + SG * a.splits - 1) / (SG * a.splits));
+    const dim3 grid((unsigned)((N + BM - 1) / BM), (unsigned)(mp / NT), (unsigned)a.splits);
+    switch (NT) {
+        case 16: return dots ? launch_nt<16, true>(tw, tx, tsw, tsx, a, grid, stream)
+                             : launch_nt<16, false>(tw, tx, tsw, tsx, a, grid, stream);
+        case 32: return dots ? launch_nt<32, true>(tw, tx, tsw, tsx, a, grid, stream)
+                             : launch_nt<32, false>(tw, tx, tsw, tsx, a, grid, stream);
+        case 64: return dots ? launch_nt<64, true>(tw, tx, tsw, tsx, a, grid, stream)
+                             : launch_nt<64, false>(tw, tx, tsw, tsx, a, grid, stream);
+        default: return dots ? launch_nt<128, true>(tw, tx, tsw, tsx, a, grid, stream)
+                             : launch_nt<128, false>(tw, tx, tsw, tsx, a, grid, stream);
+    }
+}
+
+w4a8_status launch_tc_linear(const uint16_t *x, const void *packed_w, const uint16_t *scales, int M, int N, int K,
+                             uint16_t *out, int32_t *dots, void *workspace, cudaStream_t stream) {
+    if (!tc_supported(M, N, K)) return W4A8_ERR_UNSUPPORTED;
+    const int mp = tc_tokens_padded(M);
+    uint16_t *q16 = static_cast<uint16_t *>(workspace);
+    float *sx = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + (size_t)mp * K * 2);
+    w4a8_status st = launch_quant_prefill(x, M, K, mp, q16, sx, stream);
+    if (st != W4A8_OK) return st;
+    return launch_tc_gemm(q16, sx, packed_w, scales, M, N, K, out, dots, stream);
+}
+
+}  // namespace w4a8_host

@@ -33,8 +33,20 @@ namespace {
 
 using namespace w4a8;
 
-constexpr int CWARPS = 8;                   // consumer warps
-constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
+// Consumer warps per CTA, and CTAs per SM the registers are capped for.
+// When a lane holds few activation-code words in registers (tokens x code
+// slices x weight rows per output <= 2), registers are capped so that three
+// launches' CTAs fit on an SM at once: each CTA's weight copies are then
+// issued two launches before its rows are needed.  (More consumer warps do
+// not help: the work after the dependency wait is issue-bound.)
+constexpr bool light_cfg(int MT, int BPL, int NV) { return MT * (BPL > 0 ? BPL : 1) * NV <= 2; }
+template <int MT, int BPL, int NV>
+struct Warps {
+    static constexpr bool LIGHT = light_cfg(MT, BPL, NV);
+    static constexpr int CW = 8;
+    static constexpr int THREADS = (CW + 1) * 32;   // + one producer warp
+    static constexpr int MIN_CTAS = LIGHT ? 3 : 1;
+};
 constexpr int STAGES = 8;
 constexpr int STAGE_TARGET = 65536;         // weight bytes per chunk (at least; fewer, larger chunks
                                             // shorten the work after the dependency wait)
@@ -109,7 +121,37 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(CWARPS * 32) : "memory"); }
+template <int CW>
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory"); }
+
+constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
+constexpr int pow2ceil(int v) { return v <= 1 ? 1 : 2 * pow2ceil((v + 1) / 2); }
+
+// Sums P per-lane values over the 32 lanes of a warp in P - 1 + 5 - log2(P)
+// shuffles: each halving step keeps one half of the lane's values (chosen by
+// the lane's bit) and sends the other half to the partner lane, which keeps
+// the opposite half; the remaining steps are plain butterflies.  Afterwards
+// every lane holds the total of value index lane >> (5 - log2(P)).
+template <int P>
+__device__ __forceinline__ float warp_reduce_halving(float (&v)[P], int lane) {
+    constexpr int L = ilog2(P);
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+        const int bit = 16 >> l;
+        const bool up = (lane & bit) != 0;
+        const int half = P >> (l + 1);
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float keep = up ? v[i + half] : v[i];
+            const float send = up ? v[i] : v[i + half];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (int bit = 16 >> L; bit > 0; bit >>= 1) t += __shfl_xor_sync(0xffffffffu, t, bit);
+    return t;
+}
 
 // BPL > 0: K has BPL slices of 32 blocks and each lane keeps the activation
 // codes of its BPL blocks in registers.  BPL == 0: any K; the codes are read
@@ -121,9 +163,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 // Q8: the activations arrive already quantised (int8 codes and fp32 block
 // scales, e.g. from the RMS-normalisation operator) instead of as fp16 x.
 template <int MT, int BPL, bool DEBUG, bool GATED, bool Q8>
-__global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
+__global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<MT, BPL, GATED ? 2 : 1>::MIN_CTAS)
+    gemv_stream_kernel(StreamArgs a) {
     static_assert(!(DEBUG && GATED) && !(DEBUG && Q8), "the debug instantiation is the plain linear");
     constexpr int NV = GATED ? 2 : 1;         // weight rows per output row
+    constexpr int CWARPS = Warps<MT, BPL, NV>::CW;
     constexpr int RG = (8 / MT) < RG_MAX ? (8 / MT) : RG_MAX;
     const int rgr = a.rg;
     extern __shared__ __align__(16) uint8_t smem[];
@@ -240,7 +284,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
             }
         }
     }
-    consumer_sync();
+    consumer_sync<CWARPS>();
 
     // this lane's K blocks (lane + 32 j) and their activation codes, in registers
     constexpr int BR = BPL > 0 ? BPL : 1;
@@ -289,38 +333,40 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
             const int rb = base + warp * rgp;
             base += CWARPS * rgp;
             if (rb >= rows) continue;
-            float v[RG * NV][MT];      // [output row g][branch] flattened
+            // partial sums of this lane: value (g * MT + m) * NV + br is output
+            // row rb + g, token m, branch br (0 gate or plain, 1 up)
+            constexpr int NVAL = RG * MT * NV;
+            constexpr int P = pow2ceil(NVAL);
+            float v[P];
 #pragma unroll
-            for (int g = 0; g < RG * NV; ++g)
-#pragma unroll
-                for (int m = 0; m < MT; ++m) v[g][m] = 0.0f;
-            // one 32-block of a weight row (weights at wp, scale swh) against every token
-            auto block = [&](int g, int n, int b, const uint8_t *wp, uint16_t swh, const uint32_t (*q)[8],
+            for (int i = 0; i < P; ++i) v[i] = 0.0f;
+            // one 32-block of a weight row (weights at wp, scale swh) against
+            // every token.  Even k sit in the low nibbles, odd k in the high
+            // nibbles: masking the high nibbles in place gives 16x the odd
+            // weights, so they run in their own dp4a chain, divided by 16
+            // (exactly) when the block is done.
+            auto block = [&](int g, int br, int n, int b, const uint8_t *wp, uint16_t swh, const uint32_t (*q)[8],
                              const float *sxv, const int *cbv) {
                 const uint4 w = *reinterpret_cast<const uint4 *>(wp);
                 const float swf = __half2float(__ushort_as_half(swh));
                 const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-                uint32_t lo[4], hi[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    lo[i] = nib_even(w4[i]);
-                    hi[i] = nib_odd(w4[i]);
-                }
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    int d = cbv[m];
+                    int de = cbv[m], d16 = 0;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        d = dp4a_us(lo[i], q[m][2 * i], d);
-                        d = dp4a_us(hi[i], q[m][2 * i + 1], d);
+                        de = dp4a_us(w4[i] & 0x0F0F0F0Fu, q[m][2 * i], de);
+                        d16 = dp4a_us(w4[i] & 0xF0F0F0F0u, q[m][2 * i + 1], d16);
                     }
+                    const int d = de + (d16 >> 4);
                     if (DEBUG && m < a.M) a.dots[((size_t)m * a.N + n) * a.nb + b] = d - kMagicBits;
-                    v[g][m] = fmaf(__int_as_float(d) - kMagic, swf * sxv[m], v[g][m]);
+                    float &acc = v[(g * MT + m) * NV + br];
+                    acc = fmaf(__int_as_float(d) - kMagic, swf * sxv[m], acc);
                 }
             };
 #pragma unroll
             for (int gv = 0; gv < RG * NV; ++gv) {
-                const int g = gv / NV, br = gv % NV;   // output row, branch (0 gate / plain, 1 up)
+                const int g = gv / NV, br = gv % NV;
                 const int rr = rb + g;
                 if (g >= rgp || rr >= rows) break;
                 const int n = r0 + c * a.cr + rr;
@@ -343,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
                                 sxv[m] = sxr[m][j];
                                 cbv[m] = cbr[m][j];
                             }
-                            block(gv, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
+                            block(g, br, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
                         }
                     }
                 } else {
@@ -361,26 +407,17 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_stream_kernel(StreamArgs a) {
                             sxv[m] = sxs[m * a.nb + b];
                             cbv[m] = cbs[m * a.nb + b];
                         }
-                        block(gv, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
+                        block(g, br, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
                     }
                 }
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                for (int g = 0; g < RG * NV; ++g)
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) v[g][m] += __shfl_xor_sync(0xffffffffu, v[g][m], o);
-            // lane g*MT + m stores row rb+g, token m
-            float mine = 0.0f;
-#pragma unroll
-            for (int g = 0; g < RG; ++g)
-#pragma unroll
-                for (int m = 0; m < MT; ++m)
-                    if (lane == g * MT + m) mine = GATED ? gate_act(a.act, v[g * NV][m]) * v[g * NV + NV - 1][m] : v[g][m];
-            const int g = lane / MT, m = lane - (lane / MT) * MT;
-            if (lane < rgp * MT && rb + g < rows && m < a.M)
-                a.out[(size_t)m * a.N + r0 + c * a.cr + rb + g] = __half_as_ushort(__float2half_rn(mine));
+            float t = warp_reduce_halving<P>(v, lane);
+            constexpr int SH = 5 - ilog2(P);             // lanes per value after the reduction: 1 << SH
+            const int vi = lane >> SH;
+            if constexpr (GATED) t = gate_act(a.act, t) * __shfl_xor_sync(0xffffffffu, t, 1 << SH);
+            const int br = vi % NV, g = (vi / NV) / MT, m = (vi / NV) % MT;
+            if ((lane & ((1 << SH) - 1)) == 0 && vi < NVAL && br == 0 && g < rgp && rb + g < rows && m < a.M)
+                a.out[(size_t)m * a.N + r0 + c * a.cr + rb + g] = __half_as_ushort(__float2half_rn(t));
         }
         if (reuse) {
             __syncwarp();
@@ -403,8 +440,7 @@ constexpr int kSMs = 152;
 // quarter of the CTA's bytes (at least 64 KB, so a CTA of up to 64 KB is one
 // chunk).  When the ring does not fit,
 // fewer slots are tried before smaller chunks (down to two slots), first
-// within the co-resident budget, then with one CTA per SM; rows per warp and
-// pass (rg) shrink until a chunk keeps all eight consumer warps busy.
+// within the co-resident budget, then with one CTA per SM.
 Plan make_plan(int M, int N, int K, int nv = 1) {
     // nv = weight rows per output row (2 for the gated kernel)
     Plan p{};
@@ -434,20 +470,21 @@ Plan make_plan(int M, int N, int K, int nv = 1) {
         }
         return p.smem <= limit;
     };
+    const int cw = Warps<1, 1, 1>::CW;
     bool ok = false;
     for (size_t limit : {(size_t)SMEM_COTENANT, (size_t)SMEM_ALONE}) {
         for (int cr = cr0; cr >= 1 && !ok; cr = (cr == 1 ? 0 : (cr + 1) / 2)) {
             ok = fit(cr, limit);
-            if (ok && cr < CWARPS && cr < cr0 && limit == SMEM_COTENANT) ok = false;   // try one CTA per SM first
+            if (ok && cr < cw && cr < cr0 && limit == SMEM_COTENANT) ok = false;   // try one CTA per SM first
         }
         if (ok) break;
     }
     if (!ok) {   // last resort: the smallest ring that fits alone
         for (int cr = cr0; cr >= 1 && !ok; cr = (cr == 1 ? 0 : (cr + 1) / 2)) ok = fit(cr, SMEM_ALONE);
     }
-    const int rg_cap = (8 / p.MT) < RG_MAX ? (8 / p.MT) : RG_MAX;
-    p.rg = rg_cap;
-    while (p.rg > 1 && p.cr < CWARPS * p.rg) p.rg /= 2;
+    // rows per warp and pass: the kernel spreads each pass's rows over all
+    // consumer warps (at most this many per warp)
+    p.rg = (8 / p.MT) < RG_MAX ? (8 / p.MT) : RG_MAX;
     p.ok = ok;
     return p;
 }
@@ -460,7 +497,7 @@ w4a8_status launch_t(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
     if (ast != W4A8_OK) return ast;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -51,12 +51,29 @@ w4a8_status launch_gemv_stream(const uint16_t *x, const void *packed_w, const ui
 size_t prefill_workspace_bytes(int M, int N, int K);
 // The GEMM alone, on activations already in the prefill layout: q16 fp16
 // codes [Mp][K] (k permuted 0,4,1,5,2,6,3,7 in every 8) and sx fp32 [K/32][Mp],
-// Mp = M rounded up to 128 (rows past M zero).
+// Mp = prefill_tokens_padded(M, N, K) (rows past M zero).
 w4a8_status launch_prefill_gemm(const uint16_t *q16, const float *sx, const void *packed_w, const uint16_t *scales,
                                 int M, int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream);
 
-// CTAs along K per output tile of the prefill GEMM (1, 2, 4 or 8).
+// CTAs along K per output tile of the prefill GEMM (1, 2, 4 or 8), and the
+// token rows its quantised activations are padded to.
 int prefill_splits(int M, int N, int K);
+int prefill_tokens_padded(int M, int N, int K);
+
+// Tensor-core linear with the weights as the 128-row MMA operand
+// (gemm_mid.cu): tokens as the MMA's N, in tiles of 16, 32 or 64 (one tile,
+// M <= 64: the short-sequence path) or 128 (longer sequences), after the
+// quantisation pass into `workspace` (fp16 codes [Mp][K], scales [K/32][Mp],
+// Mp = tc_tokens_padded(M)).  Needs K % 256 == 0.
+bool tc_supported(int M, int N, int K);
+bool mid_supported(int M, int N, int K);
+int tc_tokens_padded(int M);
+int tc_splits(int M, int N, int K);
+size_t tc_workspace_bytes(int M, int N, int K);
+w4a8_status launch_tc_gemm(const uint16_t *q16, const float *sx, const void *packed_w, const uint16_t *scales, int M,
+                           int N, int K, uint16_t *out, int32_t *dots, cudaStream_t stream);
+w4a8_status launch_tc_linear(const uint16_t *x, const void *packed_w, const uint16_t *scales, int M, int N, int K,
+                             uint16_t *out, int32_t *dots, void *workspace, cudaStream_t stream);
 
 // RMS normalisation (+ residual) emitting activation codes (norm.cu), and the
 // linear on such codes (decode GEMV when it takes the shape, else conversion

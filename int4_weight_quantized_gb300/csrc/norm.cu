@@ -145,7 +145,7 @@ w4a8_status launch_linear_q8(const int8_t *codes, const float *sx, const void *p
         return launch_gemv_stream_q8(codes, sx, packed_w, scales, M, N, K, out, stream);
     const size_t need = prefill_workspace_bytes(M, N, K);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return W4A8_ERR_WORKSPACE;
-    const int mp = (M + 127) / 128 * 128;
+    const int mp = prefill_tokens_padded(M, N, K);
     uint16_t *q16 = static_cast<uint16_t *>(workspace);
     float *sxt = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + (size_t)mp * K * 2);
     const long long items = (long long)mp * (K / 32) * 4;

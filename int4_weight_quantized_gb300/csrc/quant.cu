@@ -39,6 +39,9 @@ __global__ void __launch_bounds__(256) quant_debug_kernel(const uint16_t *__rest
 // [K/32][Mp].  Token rows M..Mp-1 are written as zeros (codes and scales).
 __global__ void __launch_bounds__(256) quant_prefill_kernel(const uint16_t *__restrict__ x, int M, int K, int Mp,
                                                             uint16_t *__restrict__ q16, float *__restrict__ sx) {
+    // The GEMM that reads this pass's output may start now and prefetch its
+    // weights; it waits for this grid to finish before reading the codes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int nb = K / kBlock;
     const long long items = (long long)Mp * nb * 4;
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;

@@ -52,19 +52,32 @@ def test_packed_bytes(L):
 
 
 def test_stage_aware_dispatch(L):
-    # decode for a handful of tokens, prefill for a sequence
-    for M in range(1, 9):
+    # decode for one or two tokens, the short-sequence tensor-core kernel up
+    # to 64 tokens, prefill for a sequence
+    for M in (1, 2):
         assert L.w4a8_select_path(M, 8192, 2048) == 1
-    for M in (9, 16, 64, 512):
+    for M in (3, 4, 8, 9, 16, 33, 64):
+        assert L.w4a8_select_path(M, 8192, 2048) == 3
+    for M in (65, 128, 512):
         assert L.w4a8_select_path(M, 8192, 2048) == 2
+    # the mid path needs K % 256 == 0; decode keeps up to 8 tokens otherwise
+    assert L.w4a8_select_path(4, 8192, 2080) == 1
+    assert L.w4a8_select_path(16, 8192, 2080) == 2
     assert L.w4a8_select_path(0, 8192, 2048) == 0
     assert L.w4a8_select_path(1, 8192, 2000) == 0
+    # splits of the mid path: K spread over more CTAs when there are few tiles
+    assert L.w4a8_mid_splits(8, 4096, 14336) >= 2
+    assert L.w4a8_mid_splits(8, 8192, 2080) == 0
 
 
 def test_workspace_sizes(L):
+    L.w4a8_workspace_bytes.restype = ctypes.c_size_t
     assert L.w4a8_workspace_bytes(1, 8192, 2048, 1) == 0
     assert L.w4a8_workspace_bytes(1, 8192, 2048, 0) == 0
     assert L.w4a8_workspace_bytes(0, 8192, 2048, 2) == 0
+    # mid path: fp16 codes [Mp][K] + fp32 scales [K/32][Mp], Mp = 16, 32 or 64
+    assert L.w4a8_workspace_bytes(5, 8192, 2048, 3) == 16 * 2048 * 2 + 64 * 16 * 4
+    assert L.w4a8_workspace_bytes(40, 8192, 2048, 0) == 64 * 2048 * 2 + 64 * 64 * 4
 
 
 def test_bad_arguments_rejected_before_launch(L):
@@ -131,5 +144,6 @@ def test_new_workspace_sizes(L):
     assert nb >= 4 * 8 * 2 * 256 * 4 + 4 * 8 * 2 * 2 * 4
     assert L.w4a8_decode_attention_workspace_bytes(4, 8, 3, 256, 129) == 0      # invalid: 8 % 3
     assert L.w4a8_prefill_splits(512, 8192, 2048) == 1
-    assert L.w4a8_prefill_splits(16, 128, 1024) == 8
+    assert L.w4a8_prefill_splits(16, 128, 1056) == 8      # K % 256 != 0: the 128 x 128-tile kernel
+    assert L.w4a8_prefill_splits(100, 256, 4096) == 8     # 128-token tiles of the streaming kernel
     assert L.w4a8_prefill_splits(0, 128, 1024) == 0

@@ -114,9 +114,12 @@ def test_block_dots_bit_exact(w4, path, M, N, K):
 
 
 # shapes whose prefill tiles run as 1, 2, 4 and 8 CTAs along K (cluster
-# split-K with a fixed-order reduction in distributed shared memory)
-SPLIT_SHAPES = [((200, 10240, 256), 1), ((65, 8192, 512), 2), ((33, 2560, 1024), 4), ((16, 128, 1024), 8),
-                ((130, 70, 320), 4)]
+# split-K with a fixed-order reduction in distributed shared memory): with
+# K % 256 != 0 they take the 128 x 128-tile kernel, otherwise the kernel with
+# the weights as the 128-row operand and 128-token tiles
+SPLIT_SHAPES = [((200, 10240, 288), 1), ((65, 8192, 544), 2), ((33, 2560, 1056), 4), ((16, 128, 1056), 8),
+                ((130, 70, 320), 4), ((65, 8192, 512), 1), ((129, 300, 1024), 2), ((200, 1024, 2048), 4),
+                ((100, 256, 4096), 8), ((512, 256, 14336), 4)]
 
 
 @pytest.mark.parametrize("shape,splits", SPLIT_SHAPES)
@@ -132,6 +135,35 @@ def test_prefill_split_k_bit_exact(w4, shape, splits):
     ref = oracle.linear(x.numpy(), codes.numpy(), scales.numpy())
     assert_fp16_close(_np(y), ref, f"debug {M}x{N}x{K}")
     assert_fp16_close(_np(w4.linear(xd, packed, sd, path=2)), ref, f"linear {M}x{N}x{K}")
+
+
+# the short-sequence tensor-core path (weights as the 128-row operand, tokens
+# padded to 16, 32 or 64): token counts on both sides of each padding step,
+# ragged N (partial last 128-row tile), and K split over 1, 2, 4 and 8 CTAs
+MID_SHAPES = [(1, 130, 256), (3, 300, 1024), (8, 1000, 2048), (9, 129, 512), (16, 64, 4096), (17, 257, 768),
+              (33, 200, 2048), (64, 520, 1024), (40, 4096, 14336), (5, 128, 8192), (64, 77, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", MID_SHAPES)
+def test_mid_path_bit_exact(w4, M, N, K):
+    x = wl.make_x(M, K, seed=1500 + M, outlier_frac=0.01)
+    codes, scales = wl.make_weights(N, K, seed=1600 + N, s_lo=-0.01, s_hi=0.01)
+    xd, packed, sd = _setup(w4, x, codes, scales)
+    dots, y = w4.debug_block_dots(xd, packed, sd, path=w4.PATH_MID)
+    q, _ = oracle.quantize_act(x.numpy())
+    assert np.array_equal(_np(dots), oracle.block_dots(q, codes.numpy()))
+    ref = oracle.linear(x.numpy(), codes.numpy(), scales.numpy())
+    assert_fp16_close(_np(y), ref, f"mid debug {M}x{N}x{K}")
+    y2 = w4.linear(xd, packed, sd, path=w4.PATH_MID)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    assert w4.get_device_status() == 0
+
+
+def test_mid_path_split_counts(w4):
+    """The shapes above reach every split count of the mid path."""
+    seen = {w4.mid_splits(M, N, K) for (M, N, K) in MID_SHAPES}
+    assert {1, 2, 4, 8} <= seen, seen
 
 
 # --------------------------------------------------------- gated pair
@@ -301,7 +333,7 @@ def test_linear_edge_shapes(w4, M, N, K):
     assert_fp16_close(_np(y), oracle.linear(x.numpy(), codes.numpy(), scales.numpy()), f"{M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_linear_zero_inputs(w4, path):
     M, N, K = 12, 96, 256
     x = wl.make_x(M, K, seed=5)
@@ -327,8 +359,10 @@ def test_paths_agree_on_integer_work(w4, M):
     xd, packed, sd = _setup(w4, x, codes, scales)
     d1, y1 = w4.debug_block_dots(xd, packed, sd, path=1)
     d2, y2 = w4.debug_block_dots(xd, packed, sd, path=2)
-    assert torch.equal(d1, d2)
+    d3, y3 = w4.debug_block_dots(xd, packed, sd, path=3)
+    assert torch.equal(d1, d2) and torch.equal(d1, d3)
     assert_fp16_close(_np(y1), _np(y2))
+    assert_fp16_close(_np(y3), _np(y2))
 
 
 def test_c_entry_point_matches_ex(w4):
