@@ -96,10 +96,11 @@ size_t w4a8_packed_bytes(int N, int K);
 w4a8_status w4a8_pack(const int8_t *w_codes, int N, int K, void *packed_w,
                       cudaStream_t stream);
 
-/* The kernel w4a8_linear would run for this shape: W4A8_PATH_DECODE for one
- * or two tokens, W4A8_PATH_MID for 3 to 64 tokens (when K % 256 == 0; else
- * decode up to 8 tokens), W4A8_PATH_PREFILL above.  Returns W4A8_PATH_AUTO
- * (0) for an invalid shape. */
+/* The kernel w4a8_linear would run for this shape: W4A8_PATH_DECODE for up
+ * to 3 tokens (4 when K < 12288), W4A8_PATH_MID from there to 64 tokens
+ * (when K % 256 == 0; else decode up to 8 tokens), W4A8_PATH_PREFILL above
+ * (thresholds measured on GB300).  Returns W4A8_PATH_AUTO (0) for an
+ * invalid shape. */
 int w4a8_select_path(int M, int N, int K);
 
 /* Number of CTAs along K per 128-row tile that W4A8_PATH_MID uses for this

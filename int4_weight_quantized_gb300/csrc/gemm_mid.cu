@@ -13,13 +13,16 @@
 // tensor cores do the block dots and the weights are read once.
 //
 // Per CTA (128 weight rows, a range of K, all tokens):
-//   - warp 0 streams the packed int4 weight tiles (128 rows x 64 k = 4 KB)
-//     by TMA into a 16-deep ring; it starts before the kernel waits for the
-//     quantisation pass (programmatic dependent launch);
+//   - warp 0 streams the packed int4 weight tiles by TMA, 128 rows x 128
+//     bytes (four 64-k stages) per load, into a ring of 2-4 such tiles; it
+//     starts before the kernel waits for the quantisation pass (programmatic
+//     dependent launch).  Tiles of 32-byte rows stream at well under half the
+//     rate of 128-byte rows (measured), hence the wide loads;
 //   - warps 4-7 expand them into fp16 (exact: -8..7) in the 128-byte-swizzled
 //     K-major layout of the MMA's A operand;
 //   - warp 3 loads the activation codes (fp16, written by the quantisation
-//     pass) as the B operand, warp 2 the block scales s_w and s_x;
+//     pass) as the B operand, warp 2 the block scales s_w (64 blocks of each
+//     row per load) and s_x;
 //   - warp 1 issues tcgen05.mma (M = 128 rows, N = tokens, K = 16), two per
 //     32-block, each block into its own TMEM accumulator of N columns; four
 //     accumulator units of 128 columns cycle between it and the epilogue;
@@ -46,32 +49,42 @@ using namespace w4a8;
 constexpr int BM = 128;           // weight rows per CTA: MMA M, TMEM lanes
 constexpr int KS = 64;            // k per stage: two 32-blocks
 constexpr int AS = 4;             // fp16 weight (A operand) stages
-constexpr int XS = 4;             // activation (B operand) stages
-constexpr int SG = 16;            // 32-blocks per scale load
-constexpr int SS = 3;             // scale stages
+constexpr int PS = AS / 2;        // stage pairs of A tiles in flight (one barrier per pair)
+constexpr int WSTG = 4;           // pipeline stages per packed-weight load (128 bytes of each row)
+constexpr int SG = 16;            // 32-blocks per s_x load
+constexpr int SS = 3;             // s_x stages
+constexpr int SWG = 64;           // 32-blocks per s_w load (128 bytes of each row)
+constexpr int SWS = 2;            // s_w stages
 constexpr int UNITS = 4;          // TMEM accumulator units of 128 columns (all 512)
 constexpr int A_TILE = BM * KS * 2;            // 16 KB
-constexpr int W_TILE = BM * KS / 2;            // 4 KB
-constexpr int SW_TILE = BM * SG * 2;           // 4 KB
+constexpr int W_TILE = BM * 128;               // 16 KB: 128 rows x 128 bytes (4 stages), 128-byte swizzle
+constexpr int SW_TILE = BM * SWG * 2;          // 16 KB: 128 rows x 64 fp16, 128-byte swizzle
 constexpr int CONV_WARP0 = 4;
-constexpr int EPI_WARP0 = 8;
 constexpr int EPI_WARPS = 8;      // 2 per TMEM lane quarter, half of the tokens each
-constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
 
 template <int NT>
 struct Layout {
-    static constexpr int WS = NT == 128 ? 8 : 16;          // packed weight stages (4 KB each)
+    static constexpr int WS = NT == 128 ? 2 : 4;           // packed-weight slots (4 pipeline stages each)
     static constexpr int X_TILE = NT * KS * 2;            // NT tokens x 64 k fp16
+    // activation stages: a ring of its own, deep enough to hide the load
+    // latency (about a microsecond) behind the MMAs of several stages
+    static constexpr int XS = NT == 16 ? 16 : (NT == 32 ? 12 : (NT == 64 ? 6 : 4));
+    static constexpr int XP = XS / 2;                      // activation stage pairs (one barrier each)
     static constexpr int SX_TILE = SG * NT * 4;            // 16 blocks x NT tokens fp32
     static constexpr int UB = 128 / NT;                    // blocks per accumulator unit
+    // int4 -> fp16 expansion warps (one thread per weight row; 8 warps with
+    // two threads per row measured no faster)
+    static constexpr int CONVW = 4;
+    static constexpr int EPI0 = CONV_WARP0 + CONVW;        // first epilogue warp (a multiple of 4)
+    static constexpr int THREADS = (EPI0 + EPI_WARPS) * 32;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_X = OFF_A + AS * A_TILE;
     static constexpr int OFF_W = OFF_X + XS * X_TILE;
     static constexpr int OFF_SW = OFF_W + WS * W_TILE;
-    static constexpr int OFF_SX = OFF_SW + SS * SW_TILE;
+    static constexpr int OFF_SX = OFF_SW + SWS * SW_TILE;
     static constexpr int OFF_BAR = OFF_SX + SS * SX_TILE;
-    // wfull, wempty; afull, aempty; xfull, xempty; sfull, sempty; accfull, accempty; final
-    static constexpr int NUM_BARS = 2 * WS + 2 * AS + 2 * XS + 2 * SS + 2 * UNITS + 1;
+    // wfull, wempty; pfull, pempty; xfull, xempty; sfull, sempty (s_x); swfull, swempty; accfull, accempty; final
+    static constexpr int NUM_BARS = 2 * WS + 2 * PS + 2 * XP + 2 * SS + 2 * SWS + 2 * UNITS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;     // + slack to align the base to 1024
     static_assert(128 * NT * 4 <= AS * A_TILE, "split-K partial tile must fit the A ring");
@@ -94,7 +107,7 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 // wait raises the CTA's abort flag; once it is up, waits fail at once.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const MidArgs &a,
                                           volatile uint32_t *abort_flag) {
-    bool ok = (*abort_flag == 0u) && (mbar_test_wait(bar, parity) || mbar_wait_bounded(bar, parity, a.budget, a.status));
+    bool ok = mbar_test_wait(bar, parity) || ((*abort_flag == 0u) && mbar_wait_bounded(bar, parity, a.budget, a.status));
     ok = __all_sync(0xffffffffu, ok);
     if (!ok && (threadIdx.x & 31) == 0) *abort_flag = 1u;
     return ok;
@@ -102,8 +115,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
 
 // Single-thread bounded wait; raises the abort flag on failure.
 __device__ __forceinline__ bool one_wait(uint64_t *bar, uint32_t parity, const MidArgs &a, volatile uint32_t *abort_flag) {
+    if (mbar_test_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (mbar_test_wait(bar, parity) || mbar_wait_bounded(bar, parity, a.budget, a.status)) return true;
+    if (mbar_wait_bounded(bar, parity, a.budget, a.status)) return true;
     *abort_flag = 1u;
     return false;
 }
@@ -157,11 +171,12 @@ __device__ __forceinline__ void scale_acc(float2 *acc, const uint32_t *d, float 
 }
 
 template <int NT, bool DEBUG>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Layout<NT>::THREADS, 1)
 gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                 const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_sx, MidArgs a) {
     using LY = Layout<NT>;
     constexpr int WS = LY::WS;
+    constexpr int XS = LY::XS, XP = LY::XP;
     constexpr int UB = LY::UB;
     constexpr int HT = NT / 2;                 // tokens per epilogue thread
     extern __shared__ uint8_t smem_raw[];
@@ -170,10 +185,11 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
     const uint32_t sbase = smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + LY::OFF_BAR);
     uint64_t *wfull = bars, *wempty = wfull + WS;
-    uint64_t *afull = wempty + WS, *aempty = afull + AS;
-    uint64_t *xfull = aempty + AS, *xempty = xfull + XS;
-    uint64_t *sfull = xempty + XS, *sempty = sfull + SS;
-    uint64_t *accfull = sempty + SS, *accempty = accfull + UNITS;
+    uint64_t *pfull = wempty + WS, *pempty = pfull + PS;
+    uint64_t *xfull = pempty + PS, *xempty = xfull + XP;
+    uint64_t *sfull = xempty + XP, *sempty = sfull + SS;
+    uint64_t *swfull = sempty + SS, *swempty = swfull + SWS;
+    uint64_t *accfull = swempty + SWS, *accempty = accfull + UNITS;
     uint64_t *finalb = accempty + UNITS;
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + LY::OFF_MISC);   // [0] tmem, [1] abort
 
@@ -187,10 +203,13 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
     const int ngroups = (nbl + SG - 1) / SG;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < WS; ++s) { mbar_init(&wfull[s], 1); mbar_init(&wempty[s], 4); }
-        for (int s = 0; s < AS; ++s) { mbar_init(&afull[s], 4); mbar_init(&aempty[s], 1); }
-        for (int s = 0; s < XS; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
+        for (int s = 0; s < WS; ++s) { mbar_init(&wfull[s], 1); mbar_init(&wempty[s], LY::CONVW); }
+        // a pair is ready for the MMA once the 4 expansion warps have written
+        // its A tiles and seen its activation tiles land
+        for (int s = 0; s < PS; ++s) { mbar_init(&pfull[s], LY::CONVW); mbar_init(&pempty[s], 1); }
+        for (int s = 0; s < XP; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xempty[s], 1); }
         for (int s = 0; s < SS; ++s) { mbar_init(&sfull[s], 1); mbar_init(&sempty[s], EPI_WARPS); }
+        for (int s = 0; s < SWS; ++s) { mbar_init(&swfull[s], 1); mbar_init(&swempty[s], EPI_WARPS); }
         for (int s = 0; s < UNITS; ++s) { mbar_init(&accfull[s], 1); mbar_init(&accempty[s], EPI_WARPS); }
         mbar_init(finalb, 1);
         misc[1] = 0;
@@ -204,77 +223,102 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
 
     if (warp == 0) {
         // ---------------------------------------------------------- weights (TMA), before the dependency wait
+        // each load brings 128 bytes (256 k, four stages) of all 128 rows:
+        // tiles of wide rows stream at the full rate, narrow ones do not
         if (lane == 0) {
             int issued = 0;
-            for (int s = 0; s < nst; ++s) {
-                const int slot = s % WS;
-                if (!one_wait(&wempty[slot], ((uint32_t)(s / WS) & 1u) ^ 1u, a, misc + 1)) break;
+            const int nw = nst / WSTG;
+            for (int w = 0; w < nw; ++w) {
+                const int slot = w % WS;
+                if (!one_wait(&wempty[slot], ((uint32_t)(w / WS) & 1u) ^ 1u, a, misc + 1)) break;
                 mbar_arrive_expect_tx(&wfull[slot], W_TILE);
-                tma_load_2d(sbase + LY::OFF_W + slot * W_TILE, &tm_w, (b0 + 2 * s) * 16, n0, smem_u32(&wfull[slot]));
-                issued = s + 1;
+                tma_load_2d(sbase + LY::OFF_W + slot * W_TILE, &tm_w, (b0 + 2 * WSTG * w) * 16, n0, smem_u32(&wfull[slot]));
+                issued = w + 1;
             }
-            for (int s = (issued > WS ? issued - WS : 0); s < issued; ++s)
-                mbar_wait_bounded(&wfull[s % WS], (uint32_t)(s / WS) & 1u, a.budget, nullptr);
+            for (int w = (issued > WS ? issued - WS : 0); w < issued; ++w)
+                mbar_wait_bounded(&wfull[w % WS], (uint32_t)(w / WS) & 1u, a.budget, nullptr);
         }
     } else if (warp == 2 || warp == 3) {
         // ---------------------------------------------------------- scales (warp 2), activation codes (warp 3)
         pdl_wait();
-        if (lane == 0) {
-            const bool sc = warp == 2;
-            const int S = sc ? SS : XS;
-            uint64_t *fb = sc ? sfull : xfull;
-            uint64_t *eb = sc ? sempty : xempty;
-            const int nloads = sc ? ngroups : nst;
+        if (lane == 0 && warp == 3) {
             int issued = 0;
-            for (int s = 0; s < nloads; ++s) {
-                const int slot = s % S;
-                if (!one_wait(&eb[slot], ((uint32_t)(s / S) & 1u) ^ 1u, a, misc + 1)) break;
-                if (sc) {
-                    mbar_arrive_expect_tx(&fb[slot], SW_TILE + LY::SX_TILE);
-                    tma_load_2d(sbase + LY::OFF_SW + slot * SW_TILE, &tm_sw, b0 + SG * s, n0, smem_u32(&fb[slot]));
-                    tma_load_2d(sbase + LY::OFF_SX + slot * LY::SX_TILE, &tm_sx, m0, b0 + SG * s, smem_u32(&fb[slot]));
-                } else {
-                    mbar_arrive_expect_tx(&fb[slot], LY::X_TILE);
-                    tma_load_2d(sbase + LY::OFF_X + slot * LY::X_TILE, &tm_x, (b0 + 2 * s) * 32, m0, smem_u32(&fb[slot]));
+            for (int p = 0; p < nst / 2; ++p) {
+                const int slot = p % XP;
+                if (!one_wait(&xempty[slot], ((uint32_t)(p / XP) & 1u) ^ 1u, a, misc + 1)) break;
+                mbar_arrive_expect_tx(&xfull[slot], 2 * LY::X_TILE);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int st = 2 * p + h;
+                    tma_load_2d(sbase + LY::OFF_X + (st % XS) * LY::X_TILE, &tm_x, (b0 + 2 * st) * 32, m0,
+                                smem_u32(&xfull[slot]));
                 }
-                issued = s + 1;
+                issued = p + 1;
             }
-            for (int s = (issued > S ? issued - S : 0); s < issued; ++s)
-                mbar_wait_bounded(&fb[s % S], (uint32_t)(s / S) & 1u, a.budget, nullptr);
+            for (int p = (issued > XP ? issued - XP : 0); p < issued; ++p)
+                mbar_wait_bounded(&xfull[p % XP], (uint32_t)(p / XP) & 1u, a.budget, nullptr);
+        } else if (lane == 0) {
+            // s_x in groups of SG blocks; s_w (128-byte rows) once every SWG / SG groups
+            int issued = 0, swissued = 0;
+            for (int g = 0; g < ngroups; ++g) {
+                if (g % (SWG / SG) == 0) {
+                    const int w = g / (SWG / SG), slot = w % SWS;
+                    if (!one_wait(&swempty[slot], ((uint32_t)(w / SWS) & 1u) ^ 1u, a, misc + 1)) break;
+                    mbar_arrive_expect_tx(&swfull[slot], SW_TILE);
+                    tma_load_2d(sbase + LY::OFF_SW + slot * SW_TILE, &tm_sw, b0 + SWG * w, n0, smem_u32(&swfull[slot]));
+                    swissued = w + 1;
+                }
+                const int slot = g % SS;
+                if (!one_wait(&sempty[slot], ((uint32_t)(g / SS) & 1u) ^ 1u, a, misc + 1)) break;
+                mbar_arrive_expect_tx(&sfull[slot], LY::SX_TILE);
+                tma_load_2d(sbase + LY::OFF_SX + slot * LY::SX_TILE, &tm_sx, m0, b0 + SG * g, smem_u32(&sfull[slot]));
+                issued = g + 1;
+            }
+            for (int g = (issued > SS ? issued - SS : 0); g < issued; ++g)
+                mbar_wait_bounded(&sfull[g % SS], (uint32_t)(g / SS) & 1u, a.budget, nullptr);
+            for (int w = (swissued > SWS ? swissued - SWS : 0); w < swissued; ++w)
+                mbar_wait_bounded(&swfull[w % SWS], (uint32_t)(w / SWS) & 1u, a.budget, nullptr);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
+        // One barrier test and one commit per pair of stages (8 MMAs): each
+        // mbarrier round trip costs the issuing thread about as much as two
+        // MMAs of this size (measured), so they are amortised.  Descriptors
+        // are formed once; per MMA only the start-address field advances.
         if (lane == 0) {
-            const uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-            for (int s = 0; s < nst; ++s) {
-                const int as = s % AS, xs = s % XS;
-                if (!one_wait(&afull[as], (uint32_t)(s / AS) & 1u, a, misc + 1)) break;
-                if (!one_wait(&xfull[xs], (uint32_t)(s / XS) & 1u, a, misc + 1)) break;
+            constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+            const uint64_t adesc0 = smem_desc_sw128(sbase + LY::OFF_A);
+            const uint64_t xdesc0 = smem_desc_sw128(sbase + LY::OFF_X);
+            for (int p = 0; p < nst / 2; ++p) {
+                const int slot = p % PS;
+                if (!one_wait(&pfull[slot], (uint32_t)(p / PS) & 1u, a, misc + 1)) break;
+                tc_fence_after();
                 bool ok = true;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int b = 2 * s + j, u = b / UB, jj = b - u * UB;
+                for (int j = 0; j < 4; ++j) {
+                    const int st = 2 * p + (j >> 1);           // stage of this block
+                    const int b = 2 * st + (j & 1), u = b / UB, jj = b - u * UB;
                     if (jj == 0 && !one_wait(&accempty[u % UNITS], ((uint32_t)(u / UNITS) & 1u) ^ 1u, a, misc + 1)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
+                    if (jj == 0) tc_fence_after();
                     const uint32_t d = tmem + (uint32_t)((u % UNITS) * 128 + jj * NT);
-                    const uint32_t ab = sbase + LY::OFF_A + as * A_TILE + j * 64;
-                    const uint32_t xb = sbase + LY::OFF_X + xs * LY::X_TILE + j * 64;
-                    tc_mma_f16(d, smem_desc_sw128(ab), smem_desc_sw128(xb), idesc, 0u);
-                    tc_mma_f16(d, smem_desc_sw128(ab + 32), smem_desc_sw128(xb + 32), idesc, 1u);
+                    const uint64_t ao = (uint64_t)(((st % AS) * A_TILE + (j & 1) * 64) >> 4);
+                    const uint64_t xo = (uint64_t)(((st % XS) * LY::X_TILE + (j & 1) * 64) >> 4);
+                    tc_mma_f16(d, adesc0 + ao, xdesc0 + xo, idesc, 0u);
+                    tc_mma_f16(d, adesc0 + ao + 2, xdesc0 + xo + 2, idesc, 1u);
                     if (jj == UB - 1) tc_commit(smem_u32(&accfull[u % UNITS]));
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(&aempty[as]));
-                tc_commit(smem_u32(&xempty[xs]));
+                tc_commit(smem_u32(&pempty[slot]));
+                tc_commit(smem_u32(&xempty[p % XP]));
             }
             // every MMA issued so far has completed once this barrier flips
             tc_commit(smem_u32(finalb));
             mbar_wait_bounded(finalb, 0, a.budget, nullptr);
         }
-    } else if (warp >= CONV_WARP0 && warp < CONV_WARP0 + 4) {
+    } else if (warp >= CONV_WARP0 && warp < LY::EPI0) {
         // ---------------------------------------------------------- int4 -> fp16 A tiles
         // Thread r expands its row's 64 weights of the stage into 8 chunks of
         // 16 bytes, chunk c at position c ^ (r % 8) of the row's 128 bytes.
@@ -282,29 +326,44 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
         // have been used (the fp16 stores depend on them): a release right
         // after issuing the loads could let the next TMA copy into the slot
         // overtake them.
-        const int r = (warp - CONV_WARP0) * 32 + lane;
+        // The weight tile is 128-byte swizzled (chunk c of row r at c ^ (r % 8)),
+        // so a warp's reads of its 32 rows' 32 bytes spread over all banks.
+        constexpr int HALVES = LY::CONVW / 4;              // threads per weight row
+        constexpr int CW = 8 / HALVES;                     // 16-byte output chunks per thread and stage
+        const int ct = (warp - CONV_WARP0) * 32 + lane;
+        const int r = ct % 128, h = ct / 128;
         for (int s = 0; s < nst; ++s) {
-            const int ws = s % WS, as = s % AS;
-            if (!warp_wait(&wfull[ws], (uint32_t)(s / WS) & 1u, a, misc + 1)) break;
-            if (!warp_wait(&aempty[as], ((uint32_t)(s / AS) & 1u) ^ 1u, a, misc + 1)) break;
-            const uint4 *src = reinterpret_cast<const uint4 *>(smem + LY::OFF_W + ws * W_TILE + r * (KS / 2));
-            const uint4 p0 = src[0], p1 = src[1];
-            const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            const int w = s / WSTG, sub = s % WSTG, ws = w % WS, as = s % AS, p = s / 2;
+            // barrier tests cost the warp about as much as converting a
+            // stage, so each is made once per slot (weights: 4 stages) or
+            // pair (A tiles)
+            if (sub == 0 && !warp_wait(&wfull[ws], (uint32_t)(w / WS) & 1u, a, misc + 1)) break;
+            if ((s & 1) == 0 && !warp_wait(&pempty[p % PS], ((uint32_t)(p / PS) & 1u) ^ 1u, a, misc + 1)) break;
+            const uint8_t *wrow = smem + LY::OFF_W + ws * W_TILE + r * 128;
+            uint32_t wd[CW];
+#pragma unroll
+            for (int i = 0; i < CW / 4; ++i) {
+                const uint4 pk = *reinterpret_cast<const uint4 *>(wrow + (((2 * sub + h + i) ^ (r & 7)) << 4));
+                wd[4 * i] = pk.x; wd[4 * i + 1] = pk.y; wd[4 * i + 2] = pk.z; wd[4 * i + 3] = pk.w;
+            }
             uint8_t *row = smem + LY::OFF_A + as * A_TILE + r * 128;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) = int4x8_to_half8(wd[c]);
+            for (int c = 0; c < CW; ++c) {
+                const int cc = h * CW + c;                 // output chunk (8 weights) of the row
+                *reinterpret_cast<uint4 *>(row + ((cc ^ (r & 7)) << 4)) = int4x8_to_half8(wd[c]);
             }
-            fence_proxy_async_smem();
+            if (s & 1) fence_proxy_async_smem();       // both stages' tiles written: make them visible to the MMA
+            // the pair's activation tiles must have landed too before the pair is handed on
+            if ((s & 1) && !warp_wait(&xfull[p % XP], (uint32_t)(p / XP) & 1u, a, misc + 1)) break;
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&afull[as]);
-                mbar_arrive(&wempty[ws]);
+                if (s & 1) mbar_arrive(&pfull[p % PS]);
+                if (sub == WSTG - 1) mbar_arrive(&wempty[ws]);
             }
         }
-    } else if (warp >= EPI_WARP0) {
+    } else if (warp >= LY::EPI0) {
         // ---------------------------------------------------------- epilogue
-        const int e = warp - EPI_WARP0;
+        const int e = warp - LY::EPI0;
         const int q = warp & 3;                       // TMEM lane quarter this warp may access
         const int t0 = (e >> 2) * HT;                 // this warp's first token
         const int r = q * 32 + lane;
@@ -317,15 +376,22 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
         pdl_wait();                                   // outputs are written below
         for (int u = 0; u < nunits && ok; ++u) {
             const int bu = u * UB;                    // first local block of the unit
-            const int g = bu / SG;
+            const int g = bu / SG, gw = bu / SWG;
+            if (bu % SWG == 0 && !warp_wait(&swfull[gw % SWS], (uint32_t)(gw / SWS) & 1u, a, misc + 1)) {
+                ok = false;
+                break;
+            }
             if (bu % SG == 0 && !warp_wait(&sfull[g % SS], (uint32_t)(g / SS) & 1u, a, misc + 1)) {
                 ok = false;
                 break;
             }
             // this row's s_w of the unit's UB blocks (fp16 pairs), one vector load
+            // from the 128-byte-swizzled s_w tile (16-byte chunk c at c ^ (r % 8))
             uint32_t swu[UB > 1 ? UB / 2 : 1];
             {
-                const uint8_t *sp = smem + LY::OFF_SW + (g % SS) * SW_TILE + r * (SG * 2) + (bu % SG) * 2;
+                const int bo = bu % SWG;
+                const uint8_t *sp = smem + LY::OFF_SW + (gw % SWS) * SW_TILE + r * 128 + (((bo >> 3) ^ (r & 7)) << 4) +
+                                    (bo & 7) * 2;
                 if constexpr (UB == 8) {
                     const uint4 v = *reinterpret_cast<const uint4 *>(sp);
                     swu[0] = v.x; swu[1] = v.y; swu[2] = v.z; swu[3] = v.w;
@@ -359,26 +425,38 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
                     scale_acc<HT, DEBUG>(acc, d[j], sw, sxt + (bl % SG) * NT + t0, n, m0 + t0, b0 + bl, a);
                 }
             } else {
-                // one block of 128 tokens: this thread's 64 columns in two halves
+                // one block of 128 tokens: this thread's 64 columns in four
+                // chunks of 16, the next chunk's load in flight while the
+                // current one is scaled (tcgen05.wait::ld waits for all of a
+                // thread's loads, so the buffers alternate)
                 const float sw = __half2float(__ushort_as_half((uint16_t)(swu[0] & 0xffffu)));
                 const float *sxp = sxt + (bu % SG) * NT + t0;
-                uint32_t d[32];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    tmem_ld_cols<32>(tu + (uint32_t)(h * 32), d);
-                    tmem_ld_wait();
-                    if (h == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&accempty[u % UNITS]);
-                    }
-                    scale_acc<32, DEBUG>(acc + h * 16, d, sw, sxp + h * 32, n, m0 + t0 + h * 32, b0 + bu, a);
-                }
+                const int mb = m0 + t0;
+                uint32_t d0[16], d1[16];
+                tmem_ld_cols<16>(tu, d0);
+                tmem_ld_wait();
+                tmem_ld_cols<16>(tu + 16u, d1);
+                scale_acc<16, DEBUG>(acc, d0, sw, sxp, n, mb, b0 + bu, a);
+                tmem_ld_wait();
+                tmem_ld_cols<16>(tu + 32u, d0);
+                scale_acc<16, DEBUG>(acc + 8, d1, sw, sxp + 16, n, mb + 16, b0 + bu, a);
+                tmem_ld_wait();
+                tmem_ld_cols<16>(tu + 48u, d1);
+                scale_acc<16, DEBUG>(acc + 16, d0, sw, sxp + 32, n, mb + 32, b0 + bu, a);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&accempty[u % UNITS]);
+                scale_acc<16, DEBUG>(acc + 24, d1, sw, sxp + 48, n, mb + 48, b0 + bu, a);
             }
             const int bl_last = bu + UB - 1;
             if (bl_last % SG == SG - 1 || bl_last == nbl - 1) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sempty[g % SS]);
+            }
+            if (bl_last % SWG == SWG - 1 || bl_last == nbl - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&swempty[gw % SWS]);
             }
         }
         if (a.splits > 1) {
@@ -404,8 +482,8 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
         // CTA z sums tokens [z*NT/S, (z+1)*NT/S) of every peer's partial tile
         // through distributed shared memory, in split order (deterministic).
         cluster_sync_all();
-        if (warp >= EPI_WARP0) {
-            const int t = threadIdx.x - EPI_WARP0 * 32;
+        if (warp >= LY::EPI0) {
+            const int t = threadIdx.x - LY::EPI0 * 32;
             const uint32_t red = sbase + LY::OFF_A;
             const int S = a.splits;
             const int w = NT / S;                      // tokens reduced by this CTA
@@ -471,7 +549,7 @@ w4a8_status launch_nt(const CUtensorMap &tw, const CUtensorMap &tx, const CUtens
     if (ast != W4A8_OK) return ast;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(Layout<NT>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Layout<NT>::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -524,12 +602,12 @@ w4a8_status launch_tc_gemm(const uint16_t *q16, const float *sx, const void *pac
     const int NT = M <= 64 ? mp : 128;
     const int nb = K / 32;
     CUtensorMap tw, tx, tsw, tsx;
-    if (!make_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, packed_w, (uint64_t)K / 2, (uint64_t)N, KS / 2, BM,
-                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    if (!make_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, packed_w, (uint64_t)K / 2, (uint64_t)N, 128, BM,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, q16, (uint64_t)K, (uint64_t)mp, KS, NT,
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map_2d(&tsw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, (uint64_t)nb, (uint64_t)N, SG, BM,
-                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tensor_map_2d(&tsw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, scales, (uint64_t)nb, (uint64_t)N, SWG, BM,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map_2d(&tsx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sx, (uint64_t)mp, (uint64_t)nb, NT, SG,
                             CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4A8_ERR_CUDA;

@@ -52,16 +52,17 @@ def test_packed_bytes(L):
 
 
 def test_stage_aware_dispatch(L):
-    # decode for one or two tokens, the short-sequence tensor-core kernel up
-    # to 64 tokens, prefill for a sequence
-    for M in (1, 2):
+    # decode for a few tokens, the short-sequence tensor-core kernel up to
+    # 64 tokens, prefill for a sequence
+    for M in (1, 2, 3, 4):
         assert L.w4a8_select_path(M, 8192, 2048) == 1
-    for M in (3, 4, 8, 9, 16, 33, 64):
+    assert L.w4a8_select_path(4, 4096, 14336) == 3          # long rows: 4 tokens already favour the tensor cores
+    for M in (5, 8, 9, 16, 33, 64):
         assert L.w4a8_select_path(M, 8192, 2048) == 3
     for M in (65, 128, 512):
         assert L.w4a8_select_path(M, 8192, 2048) == 2
     # the mid path needs K % 256 == 0; decode keeps up to 8 tokens otherwise
-    assert L.w4a8_select_path(4, 8192, 2080) == 1
+    assert L.w4a8_select_path(6, 8192, 2080) == 1
     assert L.w4a8_select_path(16, 8192, 2080) == 2
     assert L.w4a8_select_path(0, 8192, 2048) == 0
     assert L.w4a8_select_path(1, 8192, 2000) == 0
