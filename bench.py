@@ -47,10 +47,14 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only-secondary", action="store_true",
                     help="time only the secondary workloads and print their records")
-    ap.add_argument("--secondary", default="prefill,layers,sweep,q8,attention",
+    ap.add_argument("--secondary", default="prefill,layers,sweep,q8,attention,sets32,ceiling",
                     help="comma list of secondary workloads to run: prefill, layers (both layer "
                          "workloads), layers_fused, sweep, q8 (decode on producer-quantised activations), "
-                         "attention (decode attention over an fp16 KV cache)")
+                         "attention (decode attention over an fp16 KV cache), sets32 (the headline with 32 "
+                         "rotating weight sets), ceiling (read-only HBM ceilings of the library's two load "
+                         "mechanisms)")
+    ap.add_argument("--layer-oracle-seconds", type=float, default=8.0,
+                    help="CPU budget for timing the oracle on one decoder layer (0 skips it)")
     return ap.parse_args()
 
 
@@ -337,7 +341,11 @@ def main():
 
     secondary = []
     if not args.no_secondary:
-        secondary = run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, args.secondary)
+        secondary = run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, args.secondary, headline_gbs=value)
+
+    layer_oracle = None
+    if rank == 0 and args.layer_oracle_seconds > 0 and not args.no_secondary:
+        layer_oracle = time_layer_oracle(wl, args.layer_oracle_seconds)
 
     cpu = None
     if rank == 0:
@@ -346,21 +354,155 @@ def main():
                "sample": f"{calls} whole M=1 K=2048 N=8192 calls of the plain C oracle in {secs:.1f} s, single thread"}
 
     if rank == 0:
+        summary = make_summary(value, roof, secondary, layer_oracle)
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "int4xint8", "data": "synthetic",
+                "vs_baseline": None, "dtype": "int4xint8", "data": "synthetic", "summary": summary,
                 "config": {"workload": HEADLINE, "M": lin.M, "N": lin.N, "K": lin.K, "weight_sets": S,
                            "calls_per_step": cps, "l2": f"inputs larger than L2: {S} rotating weight sets = "
                            f"{S * lin.weight_bytes / 1e6:.1f} MB > 129 MB",
                            "launch": "CUDA graph of calls_per_step decode launches", "parallelism": f"replicas{ws}"},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": args.steps * cps, "clocks": clk.summary(), "secondary": secondary}
+                "gpu_launches": args.steps * cps, "clocks": clk.summary(), "layer_oracle": layer_oracle,
+                "secondary": secondary}
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
 
 
-def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, which="prefill,layers,sweep,q8,attention"):
+def make_summary(value, roof, secondary, layer_oracle):
+    """One short record per workload (value, us, fraction of its roofline), placed
+    early in the JSON line so that a truncated copy of the line still shows it."""
+    out = {"decode_ffn_up_m1": {"GB_s": round(value, 1), "us_per_launch": round(roof["launch_time_us"], 3),
+                                "frac_hbm": round(roof["frac"], 4)}}
+    for r in secondary:
+        name = r.get("workload", "")
+        if "rows" in r:
+            for row in r["rows"]:
+                key = f"sweep_m{row['M']}_k{row['K']}_n{row['N']}"
+                out[key] = {"path": row["path"], "us": round(row["us_per_call"], 2),
+                            "frac": round(row["frac_fp16_tensor"] if row["path"] == "prefill" else row["frac_hbm"], 4)}
+            continue
+        rec = {"value": round(r["value"], 1), "unit": r["unit"].split(" ")[0]}
+        for k in ("us_per_call", "us_per_decode_step"):
+            if k in r:
+                rec["us"] = round(r[k], 2)
+        if "roofline" in r:
+            rec["frac"] = round(r["roofline"]["frac"], 4)
+        for k in ("epilogue_fp32_frac", "frac_of_bulk_read_ceiling"):
+            if k in r:
+                rec[k] = round(r[k], 4)
+        out[name] = rec
+    if layer_oracle:
+        out["decoder_layers_oracle_cpu"] = {"s_per_step_extrapolated": round(layer_oracle["s_per_step_extrapolated"], 2),
+                                            "cores": layer_oracle["cores"]}
+    return out
+
+
+def time_layer_oracle(wl, seconds):
+    """The CPU oracle on one decoder layer (7 linears, M=1) of the 26-layer
+    workload, repeated for about `seconds`; a decode step is 26 such layers and
+    the workload has 128 steps, so those totals are extrapolated (x26, x128)."""
+    import oracle
+    W = [w for w in wl.workloads() if w.name == "decoder_layers_m1_26x7"][0]
+    ins = []
+    for li, lin in enumerate(W.linears):
+        x, codes, scales = wl.make_linear_inputs(lin, W.seed + li)
+        ins.append((x.numpy(), codes.numpy(), scales.numpy()))
+    oracle.get()
+    layers, t0 = 0, time.perf_counter()
+    while True:
+        for xn, cn, sn in ins:
+            oracle.linear(xn, cn, sn)
+        layers += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    per_layer = el / layers
+    n_layers = W.extra["layers"]
+    return {"kind": "oracle", "cores": 1, "s_per_layer": per_layer, "layers_timed": layers,
+            "s_per_step_extrapolated": per_layer * n_layers,
+            "s_per_128_steps_extrapolated": per_layer * n_layers * W.extra["decode_steps"],
+            "GB_s": sum(l.bytes for l in W.linears) / per_layer / 1e9,
+            "note": "measured on one layer of the 26 (7 linears at M=1, single thread); the step (x26) and the "
+                    "128-step workload (x26x128) are extrapolations"}
+
+
+def run_sets32(w4, wl, dev, stream, hbm, peak_src, cps=512, steps=20):
+    """The headline decode shape with 32 rotating weight sets (302 MB, 2.3x the
+    L2) instead of 16, to show that the 16-set figure is not helped by L2."""
+    import torch
+    W = [w for w in wl.workloads() if w.name == HEADLINE][0]
+    lin = W.linears[0]
+    S = 32
+    xs = wl.make_x(lin.M, lin.K, W.seed, lin.outlier_frac).to(dev)
+    sets = []
+    for i in range(S):
+        c, sc = wl.make_weights_on(dev, lin.N, lin.K, W.seed + 100 + i, lin.s_lo, lin.s_hi)
+        sets.append((w4.pack(c), sc))
+        del c
+    outs = [torch.empty((lin.M, lin.N), dtype=torch.float16, device=dev) for _ in range(S)]
+    with torch.cuda.stream(stream):
+        def calls():
+            for c in range(cps):
+                i = c % S
+                w4.linear(xs, sets[i][0], sets[i][1], out=outs[i], path=w4.PATH_DECODE)
+        calls()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            calls()
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+        e1.synchronize()
+    per = e0.elapsed_time(e1) * 1e-3 / (steps * cps)
+    gbs = lin.bytes / per / 1e9
+    return {"workload": HEADLINE + "_32sets", "value": gbs, "unit": "GB/s", "us_per_call": per * 1e6,
+            "weight_set_bytes": S * lin.weight_bytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "peak_source": peak_src}}
+
+
+def run_ceiling(w4, dev, stream, hbm, headline_gbs=None, nbytes=2 << 30, reps=10):
+    """Read-only HBM ceilings of the library's two load mechanisms (bulk
+    asynchronous copies, as the decode kernel streams its weights; 128-bit
+    loads from every thread), each reading a 2 GiB buffer once per call."""
+    import torch
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    buf.fill_(1)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    res = {"workload": "hbm_read_ceiling", "bytes_per_call": nbytes}
+    with torch.cuda.stream(stream):
+        for mode, name in ((0, "bulk_copy"), (1, "ld_128")):
+            sink = torch.zeros(152, dtype=torch.int32, device=dev)
+            w4.debug_stream_read(buf, mode, sink)
+            best = None
+            for _ in range(reps):
+                flush.fill_(0)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                w4.debug_stream_read(buf, mode, sink)
+                e1.record(stream)
+                e1.synchronize()
+                ms = e0.elapsed_time(e1)
+                best = ms if best is None or ms < best else best
+            res[name + "_GB_s"] = nbytes / (best * 1e-3) / 1e9
+    res["value"] = res["bulk_copy_GB_s"]
+    res["unit"] = "GB/s"
+    res["copy_peak_GB_s"] = hbm
+    if headline_gbs:
+        res["frac_of_bulk_read_ceiling"] = headline_gbs / res["bulk_copy_GB_s"]
+    res["note"] = "best of 10 calls; the copy peak (read + write bytes) is the roofline denominator, these are context"
+    return res
+
+
+def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, which="prefill,layers,sweep,q8,attention",
+                  headline_gbs=None):
     """Secondary workloads: prefill GEMM (M=512) in TOPS, the 26-layer decode
     step and the shape sweep, each timed with CUDA events on its stream."""
     import torch
@@ -378,6 +520,10 @@ def run_secondary(w4, wl, dev, stream, hbm, bf16, peak_src, which="prefill,layer
         res.append(run_decode_q8(w4, wl, dev, stream, hbm, peak_src))
     if "attention" in which:
         res.append(run_attention(w4, dev, stream, hbm, peak_src))
+    if "sets32" in which:
+        res.append(run_sets32(w4, wl, dev, stream, hbm, peak_src))
+    if "ceiling" in which:
+        res.append(run_ceiling(w4, dev, stream, hbm, headline_gbs))
     return res
 
 
@@ -503,8 +649,17 @@ def run_prefill(w4, wl, dev, stream, bf16, peak_src):
         e1.synchronize()
     per_call = e0.elapsed_time(e1) * 1e-3 / (n * reps)
     tops = lin.ops / per_call / 1e12
+    # the per-block scaling: one multiply (s_w * s_x) and one multiply-add per
+    # output, token and 32-block, on 128 fp32 lanes per SM per clock
+    fp32_ops = 2 * lin.M * lin.N * (lin.K // 32)
+    sm_mhz = 2070.0                      # maximum SM clock of the part
+    floor_us = fp32_ops / (152 * 128 * sm_mhz * 1e6) * 1e6
     return {"workload": W.name, "value": tops, "unit": "TOPS (2*M*N*K int8-equivalent)",
                 "us_per_call": per_call * 1e6,
+                "epilogue_fp32_ops": fp32_ops, "epilogue_fp32_floor_us": floor_us,
+                "epilogue_fp32_frac": floor_us / (per_call * 1e6),
+                "epilogue_note": "floor = 2*M*N*K/32 fp32 ops at 128 lanes/clock/SM on 152 SMs at the max SM clock; "
+                                 "frac = floor / measured time",
                 "roofline": {"bound": "tensor", "achieved": tops, "peak": bf16, "unit": "TFLOP/s",
                              "frac": tops / bf16, "peak_source": peak_src,
                              "note": "contraction runs on fp16 tensor cores (exact for int4 x int8 codes); "
@@ -549,7 +704,7 @@ def run_sweep(w4, wl, dev, stream, hbm, bf16, peak_src, sets=5, reps=20):
             gbs = lin.bytes / per_call / 1e9
             tops = lin.ops / per_call / 1e12
             rows.append({"M": lin.M, "K": lin.K, "N": lin.N,
-                         "path": "decode" if path == w4.PATH_DECODE else "prefill",
+                         "path": {w4.PATH_DECODE: "decode", w4.PATH_MID: "mid"}.get(path, "prefill"),
                          "us_per_call": per_call * 1e6, "GB_s": gbs, "TOPS": tops,
                          "frac_hbm": gbs / hbm, "frac_fp16_tensor": tops / bf16})
             del ws

@@ -237,6 +237,19 @@ w4a8_status w4a8_debug_block_dots(const uint16_t *x, const void *packed_w,
                                   void *workspace, size_t workspace_bytes,
                                   cudaStream_t stream);
 
+/* Measurement aid (not part of the operator).  Decode is bound by reading
+ * the weights from memory ("Що змінює ML Drift для on-device
+ * AI-інференсу на вашому телефоні?", tech.dede.sh, section "Stage-aware
+ * оптимізація для великих мовних моделей"), so the benchmark reports the
+ * decode kernel against a read-only ceiling besides the copy peak: this
+ * reads `bytes` (a non-zero multiple of 16) at `buf` (device, 16-byte
+ * aligned) once, spread over 152 CTAs, and discards it.  mode 0 streams
+ * each CTA's slice through shared memory with bulk asynchronous copies (the
+ * decode kernel's weight stream); mode 1 uses 128-bit loads from every
+ * thread.  sink: int[152], device, zeroed by the caller (receives one word
+ * per CTA).  Asynchronous on `stream`. */
+w4a8_status w4a8_debug_stream_read(const void *buf, size_t bytes, int mode, int *sink, cudaStream_t stream);
+
 /* Prefill (tensor-core) linear that allocates nothing, for callers that
  * cannot allocate device memory: code running in a CUDA-graph node or host
  * callback, plugins of engines that own every allocation, or real-time loops

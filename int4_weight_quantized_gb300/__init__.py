@@ -73,12 +73,13 @@ def lib():
         L.w4a8_debug_quantize_act.argtypes = [P, i, i, P, P, P]
         L.w4a8_debug_block_dots.argtypes = [P, P, P, i, i, i, P, P, i, P, sz, P]
         L.w4a8_linear_prefill_noalloc.argtypes = [P, P, P, i, i, i, P, P]
+        L.w4a8_debug_stream_read.argtypes = [P, sz, i, P, P]
         L.w4a8_get_device_status.argtypes = [P]
         L.w4a8_set_wait_budget.argtypes = [ctypes.c_longlong]
         L.w4a8_debug_wait_timeout.argtypes = [P]
         for f in ("w4a8_pack", "w4a8_linear", "w4a8_linear_ex", "w4a8_linear_gated", "w4a8_rmsnorm_quant",
                   "w4a8_linear_q8", "w4a8_decode_attention", "w4a8_linear_prefill_noalloc", "w4a8_debug_quantize_act",
-                  "w4a8_debug_block_dots", "w4a8_get_device_status", "w4a8_set_wait_budget",
+                  "w4a8_debug_block_dots", "w4a8_debug_stream_read", "w4a8_get_device_status", "w4a8_set_wait_budget",
                   "w4a8_debug_wait_timeout"):
             getattr(L, f).restype = i
         _lib = L
@@ -304,6 +305,16 @@ def debug_block_dots(x, packed, scales, path=PATH_AUTO, workspace=None):
     _check(lib().w4a8_debug_block_dots(_p(x), _p(packed), _p(scales), M, N, K, _p(dots), _p(out), path,
                                        _p(workspace), wsb, _stream()), "w4a8_debug_block_dots")
     return dots, out
+
+
+def debug_stream_read(buf, mode=0, sink=None):
+    """Read the bytes of the CUDA tensor `buf` once (measurement aid: mode 0 bulk
+    copies, mode 1 128-bit loads); returns the sink tensor (int32[152])."""
+    if sink is None:
+        sink = torch.zeros(152, dtype=torch.int32, device=buf.device)
+    _check(lib().w4a8_debug_stream_read(_p(buf), buf.numel() * buf.element_size(), int(mode), _p(sink), _stream()),
+           "w4a8_debug_stream_read")
+    return sink
 
 
 def get_device_status():

@@ -25,6 +25,8 @@
 // d + 8*sum(q), and starting the integer accumulator at 0x4B400000 - 8*sum(q)
 // leaves the float 1.5*2^23 + d, from which d follows exactly by one fp32
 // subtraction.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "sync.cuh"
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<
             // weights, so they run in their own dp4a chain, divided by 16
             // (exactly) when the block is done.
             auto block = [&](int g, int br, int n, int b, const uint8_t *wp, uint16_t swh, const uint32_t (*q)[8],
-                             const float *sxv, const int *cbv) {
+                             const float *sxv, const int *cbv, bool valid) {
                 const uint4 w = *reinterpret_cast<const uint4 *>(wp);
                 const float swf = __half2float(__ushort_as_half(swh));
                 const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
@@ -359,58 +361,70 @@ __global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<
                         d16 = dp4a_us(w4[i] & 0xF0F0F0F0u, q[m][2 * i + 1], d16);
                     }
                     const int d = de + (d16 >> 4);
-                    if (DEBUG && m < a.M) a.dots[((size_t)m * a.N + n) * a.nb + b] = d - kMagicBits;
+                    if (DEBUG && valid && m < a.M) a.dots[((size_t)m * a.N + n) * a.nb + b] = d - kMagicBits;
                     float &acc = v[(g * MT + m) * NV + br];
                     acc = fmaf(__int_as_float(d) - kMagic, swf * sxv[m], acc);
                 }
             };
+            // A pass whose RG rows all exist runs without branches, so the
+            // compiler can interleave the rows' loads and dp4a chains; a
+            // shorter pass stops at its last row.  A block past the row's end
+            // reads the last block with zero codes (contributing nothing).
+            auto rows_pass = [&](auto full_tag) {
+                constexpr bool FULL = decltype(full_tag)::value;
 #pragma unroll
-            for (int gv = 0; gv < RG * NV; ++gv) {
-                const int g = gv / NV, br = gv % NV;
-                const int rr = rb + g;
-                if (g >= rgp || rr >= rows) break;
-                const int n = r0 + c * a.cr + rr;
-                const uint8_t *wrow = wst + (size_t)br * w_stage + (size_t)rr * row_bytes;
-                const uint16_t *srow = sst + (size_t)br * a.cr * a.nb + (size_t)rr * a.nb;
-                const uint16_t *sglob = a.sw + ((size_t)n + (size_t)br * a.N) * a.nb;
-                if constexpr (BPL > 0) {
-#pragma unroll
-                    for (int j = 0; j < BPL; ++j) {
-                        const int b = lane + 32 * j;
-                        if (b < a.nb) {
-                            const uint16_t swh = a.sw_bulk ? srow[b] : __ldg(sglob + b);
+                for (int gv = 0; gv < RG * NV; ++gv) {
+                    const int g = gv / NV, br = gv % NV;
+                    const int rr = rb + g;
+                    if constexpr (!FULL) {
+                        if (g >= rgp || rr >= rows) break;
+                    }
+                    const bool rvalid = true;
+                    const int n = r0 + c * a.cr + rr;
+                    const uint8_t *wrow = wst + (size_t)br * w_stage + (size_t)rr * row_bytes;
+                    const uint16_t *srow = sst + (size_t)br * a.cr * a.nb + (size_t)rr * a.nb;
+                    const uint16_t *sglob = a.sw + ((size_t)n + (size_t)br * a.N) * a.nb;
+                    if constexpr (BPL > 0) {
+    #pragma unroll
+                        for (int j = 0; j < BPL; ++j) {
+                            const int b = lane + 32 * j;
+                            const bool bvalid = b < a.nb;          // codes of such blocks are zero
+                            const int bc = bvalid ? b : a.nb - 1;
+                            const uint16_t swh = a.sw_bulk ? srow[bc] : __ldg(sglob + bc);
                             uint32_t q[MT][8];
                             float sxv[MT];
                             int cbv[MT];
-#pragma unroll
+    #pragma unroll
                             for (int m = 0; m < MT; ++m) {
-#pragma unroll
+    #pragma unroll
                                 for (int i = 0; i < 8; ++i) q[m][i] = qa[m][j][i];
                                 sxv[m] = sxr[m][j];
                                 cbv[m] = cbr[m][j];
                             }
-                            block(g, br, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
+                            block(g, br, n, bc, wrow + (size_t)bc * 16, swh, q, sxv, cbv, rvalid && bvalid);
                         }
-                    }
-                } else {
-                    for (int b = lane; b < a.nb; b += 32) {
-                        const uint16_t swh = a.sw_bulk ? srow[b] : __ldg(sglob + b);
-                        uint32_t q[MT][8];
-                        float sxv[MT];
-                        int cbv[MT];
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const uint4 *src = reinterpret_cast<const uint4 *>(codes + ((size_t)m * a.nb + b) * 8);
-                            const uint4 c0 = src[0], c1 = src[1];
-                            q[m][0] = c0.x; q[m][1] = c0.y; q[m][2] = c0.z; q[m][3] = c0.w;
-                            q[m][4] = c1.x; q[m][5] = c1.y; q[m][6] = c1.z; q[m][7] = c1.w;
-                            sxv[m] = sxs[m * a.nb + b];
-                            cbv[m] = cbs[m * a.nb + b];
+                    } else {
+                        for (int b = lane; b < a.nb; b += 32) {
+                            const uint16_t swh = a.sw_bulk ? srow[b] : __ldg(sglob + b);
+                            uint32_t q[MT][8];
+                            float sxv[MT];
+                            int cbv[MT];
+    #pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                const uint4 *src = reinterpret_cast<const uint4 *>(codes + ((size_t)m * a.nb + b) * 8);
+                                const uint4 c0 = src[0], c1 = src[1];
+                                q[m][0] = c0.x; q[m][1] = c0.y; q[m][2] = c0.z; q[m][3] = c0.w;
+                                q[m][4] = c1.x; q[m][5] = c1.y; q[m][6] = c1.z; q[m][7] = c1.w;
+                                sxv[m] = sxs[m * a.nb + b];
+                                cbv[m] = cbs[m * a.nb + b];
+                            }
+                            block(g, br, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv, rvalid);
                         }
-                        block(g, br, n, b, wrow + (size_t)b * 16, swh, q, sxv, cbv);
                     }
                 }
-            }
+            };
+            if (rgp == RG && rb + RG <= rows) rows_pass(std::true_type{});
+            else rows_pass(std::false_type{});
             float t = warp_reduce_halving<P>(v, lane);
             constexpr int SH = 5 - ilog2(P);             // lanes per value after the reduction: 1 << SH
             const int vi = lane >> SH;

@@ -99,6 +99,12 @@ def test_bad_arguments_rejected_before_launch(L):
     assert L.w4a8_debug_quantize_act(good, 1, 64, good, P(2), None) == 2
     # path argument
     assert L.w4a8_set_wait_budget(-1) == 1
+    # read-ceiling probe: sizes, mode and pointers are checked before any launch
+    L.w4a8_debug_stream_read.argtypes = [P, ctypes.c_size_t, ctypes.c_int, P, P]
+    assert L.w4a8_debug_stream_read(good, 0, 0, good, None) == 1
+    assert L.w4a8_debug_stream_read(good, 24, 0, good, None) == 1
+    assert L.w4a8_debug_stream_read(good, 4096, 2, good, None) == 1
+    assert L.w4a8_debug_stream_read(P(4097), 4096, 0, good, None) == 2
 
 
 def test_new_entry_points_reject_bad_arguments(L):
