@@ -63,9 +63,10 @@ typedef enum {
     W4A8_PATH_AUTO = 0,     /* w4a8_select_path decides */
     W4A8_PATH_DECODE = 1,   /* memory-bound GEMV, activations quantised in the kernel; M <= 8 per launch */
     W4A8_PATH_PREFILL = 2,  /* compute-bound tensor-core GEMM (tcgen05) after a quantisation pass */
-    W4A8_PATH_MID = 3       /* short sequences, M <= 64, K % 256 == 0: tensor-core kernel with the weights
-                               as the 128-row operand and the tokens (padded to 16, 32 or 64) as its N,
-                               streaming the weights once, after a quantisation pass */
+    W4A8_PATH_MID = 3       /* short sequences, M <= 64, K % 256 == 0: tensor-core kernels with the weights
+                               as the 128-row operand (held in tensor memory for up to 32 tokens) and the
+                               tokens (padded to 16, 32 or 64) as its N, streaming the weights once, after
+                               a quantisation pass */
 } w4a8_path;
 
 /* Activation of the gated pair's gate branch (w4a8_linear_gated). */
@@ -96,11 +97,11 @@ size_t w4a8_packed_bytes(int N, int K);
 w4a8_status w4a8_pack(const int8_t *w_codes, int N, int K, void *packed_w,
                       cudaStream_t stream);
 
-/* The kernel w4a8_linear would run for this shape: W4A8_PATH_DECODE for up
- * to 3 tokens (4 when K < 12288), W4A8_PATH_MID from there to 64 tokens
- * (when K % 256 == 0; else decode up to 8 tokens), W4A8_PATH_PREFILL above
- * (thresholds measured on GB300).  Returns W4A8_PATH_AUTO (0) for an
- * invalid shape. */
+/* The kernel w4a8_linear would run for this shape: W4A8_PATH_DECODE for one
+ * token, for up to 3 tokens when K <= 8192 and for 4 tokens when K <= 2048;
+ * W4A8_PATH_MID from there to 64 tokens (when K % 256 == 0; else decode up
+ * to 8 tokens); W4A8_PATH_PREFILL above (thresholds measured on GB300).
+ * Returns W4A8_PATH_AUTO (0) for an invalid shape. */
 int w4a8_select_path(int M, int N, int K);
 
 /* Number of CTAs along K per 128-row tile that W4A8_PATH_MID uses for this

@@ -122,13 +122,13 @@ size_t w4a8_packed_bytes(int N, int K) {
 
 int w4a8_select_path(int M, int N, int K) {
     if (!shape_ok(M, N, K)) return W4A8_PATH_AUTO;
-    // Thresholds measured on GB300 (decode GEMV against the short-sequence
-    // tensor-core kernel over M = 1..64 at N x K = 8192x2048, 2048x2048,
-    // 14336x4096, 4096x14336, 2048x8192): the GEMV wins up to 3 tokens, and
-    // at 4 tokens unless the rows are long; the tensor-core kernel from there
-    // to 64 tokens.
+    // Thresholds measured on GB300 (decode GEMV against the tensor-core
+    // kernels over M = 1..64 at N x K = 8192x2048, 2048x2048, 14336x4096,
+    // 4096x14336, 2048x8192): the GEMV wins at one token, and while its
+    // codes stay in registers or nearly so (up to 3 tokens with K <= 8192, 4
+    // tokens with K <= 2048); the tensor-core kernels from there to 64 tokens.
     const bool decode_ok = M <= 8 && (gemv_stream_supported(M, N, K) || gemv_supported(M, N, K));
-    if (decode_ok && (M <= 3 || (M == 4 && K < 12288))) return W4A8_PATH_DECODE;
+    if (decode_ok && (M == 1 || (M <= 3 && K <= 8192) || (M == 4 && K <= 2048))) return W4A8_PATH_DECODE;
     if (M <= 64 && mid_supported(M, N, K)) return W4A8_PATH_MID;
     if (decode_ok) return W4A8_PATH_DECODE;
     return W4A8_PATH_PREFILL;

@@ -1,5 +1,7 @@
-// gemm_mid.cu -- W4A8 linear for short sequences (3 to 64 tokens) on the
-// 5th-generation tensor cores, with the weights as the 128-row operand.
+// gemm_mid.cu -- W4A8 linear on the 5th-generation tensor cores with the
+// weights as the 128-row operand, for tiles of 64 tokens (33 to 64 tokens)
+// and of 128 tokens (prefill, K a multiple of 256); 1 to 32 tokens run in
+// gemm_small.cu.
 //
 // Stage-aware kernel choice ("Що змінює ML Drift для on-device
 // AI-інференсу на вашому телефоні?", tech.dede.sh, section "Stage-aware
@@ -8,8 +10,8 @@
 // “数据少搬”"): between one-token decode (a memory-bound GEMV) and long
 // prefill (a compute-bound GEMM) lies a range of token counts where the
 // weight stream still sets the time but dp4a per token costs too many
-// instructions.  Here the tokens are the MMA's N dimension (padded to 16, 32
-// or 64) and every CTA streams 128 weight rows through a deep ring, so the
+// instructions.  Here the tokens are the MMA's N dimension (a tile of 64 or
+// 128) and every CTA streams 128 weight rows through a deep ring, so the
 // tensor cores do the block dots and the weights are read once.
 //
 // Per CTA (128 weight rows, a range of K, all tokens):
@@ -26,7 +28,8 @@
 //   - warp 1 issues tcgen05.mma (M = 128 rows, N = tokens, K = 16), two per
 //     32-block, each block into its own TMEM accumulator of N columns; four
 //     accumulator units of 128 columns cycle between it and the epilogue;
-//   - warps 8-15 read each block's exact integer dots (tcgen05.ld) and apply
+//   - warps 8 and up (8 of them at 128 tokens, 16 at 64) read each block's
+//     exact integer dots (tcgen05.ld) and apply
 //     acc += d * (s_w * s_x) in fp32 (pairs of tokens per instruction);
 //   - with several CTAs along K (a thread-block cluster), the fp32 partial
 //     tiles are summed in a fixed order through distributed shared memory.
@@ -61,7 +64,6 @@ constexpr int A_TILE = BM * KS * 2;            // 16 KB
 constexpr int W_TILE = BM * 128;               // 16 KB: 128 rows x 128 bytes (4 stages), 128-byte swizzle
 constexpr int SW_TILE = BM * SWG * 2;          // 16 KB: 128 rows x 64 fp16, 128-byte swizzle
 constexpr int CONV_WARP0 = 4;
-constexpr int EPI_WARPS = 8;      // 2 per TMEM lane quarter, half of the tokens each
 
 template <int NT>
 struct Layout {
@@ -69,7 +71,7 @@ struct Layout {
     static constexpr int X_TILE = NT * KS * 2;            // NT tokens x 64 k fp16
     // activation stages: a ring of its own, deep enough to hide the load
     // latency (about a microsecond) behind the MMAs of several stages
-    static constexpr int XS = NT == 16 ? 16 : (NT == 32 ? 12 : (NT == 64 ? 6 : 4));
+    static constexpr int XS = NT == 64 ? 6 : 4;
     static constexpr int XP = XS / 2;                      // activation stage pairs (one barrier each)
     static constexpr int SX_TILE = SG * NT * 4;            // 16 blocks x NT tokens fp32
     static constexpr int UB = 128 / NT;                    // blocks per accumulator unit
@@ -77,6 +79,10 @@ struct Layout {
     // two threads per row measured no faster)
     static constexpr int CONVW = 4;
     static constexpr int EPI0 = CONV_WARP0 + CONVW;        // first epilogue warp (a multiple of 4)
+    // epilogue warps, a multiple of 4 (one group per TMEM lane quarter, each
+    // warp of a group a share of the tokens): 16 measured faster than 8 at
+    // 64 tokens, slower at 128
+    static constexpr int EPI_WARPS = NT == 128 ? 8 : 16;
     static constexpr int THREADS = (EPI0 + EPI_WARPS) * 32;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_X = OFF_A + AS * A_TILE;
@@ -99,7 +105,8 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
     constexpr int WS = LY::WS;
     constexpr int XS = LY::XS, XP = LY::XP;
     constexpr int UB = LY::UB;
-    constexpr int HT = NT / 2;                 // tokens per epilogue thread
+    constexpr int EPI_WARPS = LY::EPI_WARPS;
+    constexpr int HT = NT / (EPI_WARPS / 4);   // tokens per epilogue thread
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -330,7 +337,7 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
             const float *sxt = reinterpret_cast<const float *>(smem + LY::OFF_SX + (g % SS) * LY::SX_TILE);
             const uint32_t tu = tbase + (uint32_t)((u % UNITS) * 128);
             if constexpr (NT <= 64) {
-                // all UB blocks of the unit in one batch of loads (UB * HT = 64 columns)
+                // all UB blocks of the unit in one batch of loads (UB * HT columns)
                 uint32_t d[UB][HT];
 #pragma unroll
                 for (int j = 0; j < UB; ++j) tmem_ld_cols<HT>(tu + (uint32_t)(j * NT), d[j]);
@@ -346,29 +353,29 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
                     scale_acc<HT, DEBUG>(acc, d[j], sw, sxt + (bl % SG) * NT + t0, n, m0 + t0, b0 + bl, a);
                 }
             } else {
-                // one block of 128 tokens: this thread's 64 columns in four
-                // chunks of 16, the next chunk's load in flight while the
-                // current one is scaled (tcgen05.wait::ld waits for all of a
-                // thread's loads, so the buffers alternate)
+                // one block of 128 tokens: this thread's HT columns in chunks
+                // of 16, the next chunk's load in flight while the current one
+                // is scaled (tcgen05.wait::ld waits for all of a thread's
+                // loads, so the buffers alternate); the accumulator unit is
+                // released as soon as its last chunk has landed
+                constexpr int CH = HT / 16;
                 const float sw = __half2float(__ushort_as_half((uint16_t)(swu[0] & 0xffffu)));
                 const float *sxp = sxt + (bu % SG) * NT + t0;
                 const int mb = m0 + t0;
-                uint32_t d0[16], d1[16];
-                tmem_ld_cols<16>(tu, d0);
-                tmem_ld_wait();
-                tmem_ld_cols<16>(tu + 16u, d1);
-                scale_acc<16, DEBUG>(acc, d0, sw, sxp, n, mb, b0 + bu, a);
-                tmem_ld_wait();
-                tmem_ld_cols<16>(tu + 32u, d0);
-                scale_acc<16, DEBUG>(acc + 8, d1, sw, sxp + 16, n, mb + 16, b0 + bu, a);
-                tmem_ld_wait();
-                tmem_ld_cols<16>(tu + 48u, d1);
-                scale_acc<16, DEBUG>(acc + 16, d0, sw, sxp + 32, n, mb + 32, b0 + bu, a);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&accempty[u % UNITS]);
-                scale_acc<16, DEBUG>(acc + 24, d1, sw, sxp + 48, n, mb + 48, b0 + bu, a);
+                uint32_t dbuf[2][16];
+                tmem_ld_cols<16>(tu, dbuf[0]);
+#pragma unroll
+                for (int c = 0; c < CH; ++c) {
+                    tmem_ld_wait();
+                    if (c + 1 < CH) {
+                        tmem_ld_cols<16>(tu + (uint32_t)(16 * (c + 1)), dbuf[(c + 1) & 1]);
+                    } else {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&accempty[u % UNITS]);
+                    }
+                    scale_acc<16, DEBUG>(acc + 8 * c, dbuf[c & 1], sw, sxp + 16 * c, n, mb + 16 * c, b0 + bu, a);
+                }
             }
             const int bl_last = bu + UB - 1;
             if (bl_last % SG == SG - 1 || bl_last == nbl - 1) {

@@ -193,40 +193,56 @@ gemm_small_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-            const uint64_t xdesc0 = smem_desc_sw128(sbase + LY::OFF_X);
-            for (int q = 0; q < nq; ++q) {
-                const int as = q % AQ, xs = q % XQ;
-                if (!one_wait(&afull[as], (uint32_t)(q / AQ) & 1u, a, misc + 1)) break;
-                tc_fence_after();
-                bool ok = true;
+        // The whole warp runs the loop, so every address and descriptor is
+        // warp-uniform (uniform registers, computed once per quad; per block
+        // only compile-time offsets are added) and lane 0 issues.  The MMA
+        // warp shares its sub-partition with an expansion warp and two
+        // epilogue warps, so its instruction count per MMA sets its rate.
+        constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+        constexpr int UPQ = QB / UB;                  // accumulator units per quad (1 or 2)
+        const uint64_t xdesc0 = smem_desc_sw128(sbase + LY::OFF_X);
+        for (int q = 0; q < nq; ++q) {
+            const int as = q % AQ, xs = q % XQ;
+            if (!warp_wait(&afull[as], (uint32_t)(q / AQ) & 1u, a, misc + 1)) break;
+            tc_fence_after();
+            const uint32_t abase = tmem + (uint32_t)(as * 128);
+            const uint64_t xq = xdesc0 + (uint64_t)((xs * LY::X_QUAD) >> 4);
+            bool ok = true;
 #pragma unroll
-                for (int j = 0; j < QB; ++j) {
-                    const int b = QB * q + j, u = b / UB, jj = b - u * UB;
-                    if (jj == 0) {
-                        if (!one_wait(&accempty[u % UNITS], ((uint32_t)(u / UNITS) & 1u) ^ 1u, a, misc + 1)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                    }
-                    const uint32_t d = tmem + (uint32_t)(ACC0 + (u % UNITS) * 128 + jj * NT);
-                    const uint32_t at = tmem + (uint32_t)(as * 128 + j * 16);
-                    // block j of the quad: box j / 2, bytes (j % 2) * 64 of each 128-byte token row
-                    const uint64_t xo = (uint64_t)((xs * LY::X_QUAD + (j >> 1) * LY::X_BOX + (j & 1) * 64) >> 4);
-                    tc_mma_f16_ta(d, at, xdesc0 + xo, idesc, 0u);
-                    tc_mma_f16_ta(d, at + 8u, xdesc0 + xo + 2, idesc, 1u);
-                    if (jj == UB - 1) tc_commit(smem_u32(&accfull[u % UNITS]));
+            for (int h = 0; h < UPQ; ++h) {
+                const int u = q * UPQ + h;
+                if (!warp_wait(&accempty[u % UNITS], ((uint32_t)(u / UNITS) & 1u) ^ 1u, a, misc + 1)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
+                tc_fence_after();
+                const uint32_t dbase = tmem + (uint32_t)(ACC0 + (u % UNITS) * 128);
+#pragma unroll
+                for (int jj = 0; jj < UB; ++jj) {
+                    const int j = h * UB + jj;            // block of the quad
+                    // block j: box j / 2, bytes (j % 2) * 64 of each 128-byte token row
+                    const uint64_t xo = (uint64_t)((((j >> 1) * LY::X_BOX) + (j & 1) * 64) >> 4);
+                    if (lane == 0) {
+                        tc_mma_f16_ta(dbase + (uint32_t)(jj * NT), abase + (uint32_t)(j * 16), xq + xo, idesc, 0u);
+                        tc_mma_f16_ta(dbase + (uint32_t)(jj * NT), abase + (uint32_t)(j * 16 + 8), xq + xo + 2, idesc, 1u);
+                    }
+                }
+                if (lane == 0) tc_commit(smem_u32(&accfull[u % UNITS]));
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) {
                 tc_commit(smem_u32(&aempty[as]));
                 tc_commit(smem_u32(&xempty[xs]));
             }
-            // every MMA issued so far has completed once this barrier flips
+            __syncwarp();
+        }
+        // every MMA issued so far has completed once this barrier flips
+        if (lane == 0) {
             tc_commit(smem_u32(finalb));
             mbar_wait_bounded(finalb, 0, a.budget, nullptr);
         }
+        __syncwarp();
     } else if (warp >= CONV_WARP0 && warp < EPI0) {
         // ---------------------------------------------------------- int4 -> fp16 weights into tensor memory
         // Thread r holds row r: the 8 chunks of 16 bytes of its 128-byte row

@@ -57,6 +57,12 @@ def test_stage_aware_dispatch(L):
     for M in (1, 2, 3, 4):
         assert L.w4a8_select_path(M, 8192, 2048) == 1
     assert L.w4a8_select_path(4, 4096, 14336) == 3          # long rows: 4 tokens already favour the tensor cores
+    assert L.w4a8_select_path(2, 4096, 14336) == 3          # K > 8192: the GEMV's codes leave registers
+    assert L.w4a8_select_path(1, 4096, 14336) == 1
+    assert L.w4a8_select_path(3, 2048, 8192) == 1
+    assert L.w4a8_select_path(4, 2048, 8192) == 3
+    assert L.w4a8_select_path(3, 14336, 4096) == 1
+    assert L.w4a8_select_path(4, 14336, 4096) == 3
     for M in (5, 8, 9, 16, 33, 64):
         assert L.w4a8_select_path(M, 8192, 2048) == 3
     for M in (65, 128, 512):
