@@ -118,3 +118,32 @@ def test_full_shape_codes_and_dots_bit_exact(w4, case):
     yo = oracle.linear(x.numpy()[rows], codes.numpy()[cols], scales.numpy()[cols])
     assert_fp16_close(y.cpu().numpy()[np.ix_(rows, cols)], yo, case[0])
     assert w4.get_device_status() == 0
+
+
+# The sweep's two shapes at further token counts on the tensor-core path for
+# short sequences (the sweep itself runs M = 4, 8 and 64 through the dispatch
+# above): both token tiles (16 and 32 tokens with the weights in tensor
+# memory, 64 tokens in shared memory), with and without split-K.
+SWEEP_MID = [(M, N, K) for M in (3, 9, 16, 33) for (N, K) in ((14336, 4096), (4096, 14336))]
+
+
+@pytest.mark.parametrize("M,N,K", SWEEP_MID, ids=[f"m{M}_n{N}_k{K}" for (M, N, K) in SWEEP_MID])
+def test_sweep_shapes_mid_path_dots_bit_exact(w4, M, N, K):
+    x = wl.make_x(M, K, seed=2700 + M, outlier_frac=0.01)
+    codes, scales = wl.make_weights(N, K, seed=2800 + K, s_lo=0.001, s_hi=0.008)
+    xd, sd = x.cuda(), scales.cuda()
+    packed = w4.pack(codes.cuda())
+    dots, y_dbg = w4.debug_block_dots(xd, packed, sd, path=w4.PATH_MID)
+    y = w4.linear(xd, packed, sd, path=w4.PATH_MID)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(M * 7 + K)
+    cols = _sample_cols(N, g)
+    got = dots.index_select(1, torch.from_numpy(cols).cuda()).cpu().numpy()
+    del dots
+    q, _ = oracle.quantize_act(x.numpy())
+    ref = oracle.block_dots(q, codes.numpy()[cols])
+    assert np.array_equal(got, ref)
+    assert torch.equal(y, y_dbg)
+    yo = oracle.linear(x.numpy(), codes.numpy()[cols], scales.numpy()[cols])
+    assert_fp16_close(y.cpu().numpy()[:, cols], yo, f"mid {M}x{N}x{K}")
+    assert w4.get_device_status() == 0
