@@ -215,9 +215,11 @@ w4a8_status w4a8_linear_q8(const int8_t *codes, const float *sx, const void *pac
  *   out      [B][Hq][D] fp16:  out[b][h] = sum_t softmax_t(q.k_t / sqrt(D)) v_t,
  *            KV head h / (Hq/Hkv) for query head h, fp32 arithmetic.
  * Requires D in {64, 128, 256}, Hq % Hkv == 0, Hq/Hkv <= 16 and
- * Lmax <= 131072, else W4A8_ERR_INVALID_VALUE.  Sequences longer than 128 tokens are split into
- * 128-token chunks whose partial softmax sums are merged by a second kernel
- * in `workspace` (w4a8_decode_attention_workspace_bytes; 0 when none). */
+ * Lmax <= 131072, else W4A8_ERR_INVALID_VALUE.  Sequences are split into
+ * chunks (64 tokens on the tensor cores for D = 128 and 256, 128 tokens for
+ * D = 64) whose partial softmax sums are merged by a second kernel in
+ * `workspace` (w4a8_decode_attention_workspace_bytes; 0 when one chunk
+ * covers Lmax). */
 size_t w4a8_decode_attention_workspace_bytes(int B, int Hq, int Hkv, int D, int Lmax);
 w4a8_status w4a8_decode_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                                   const int32_t *lens, int B, int Hq, int Hkv, int D, int Lmax, uint16_t *out,

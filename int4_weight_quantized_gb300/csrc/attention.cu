@@ -268,12 +268,15 @@ __global__ void __launch_bounds__(NT, 2) attn_chunk_kernel(const uint16_t *__res
 // threads.  First the split weights w_s = e^(m_s - M) and L = sum l_s w_s
 // (the splits' loads spread over the threads), then each thread merges its
 // pair of dims over the splits with independent loads.
-constexpr int MAXS = 1024;      // splits per sequence the combine kernel takes (Lmax <= 131072)
+constexpr int MAXS = 2048;      // splits per sequence the combine kernel takes (Lmax <= 131072 in 64-token chunks)
 
 __global__ void attn_combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_ml, int Hq, int D,
                                     int nsplit, uint16_t *__restrict__ out) {
     __shared__ float wsh[MAXS];
     __shared__ float red[2][32];
+    // launched as a programmatic dependent of the tensor-core chunk kernel:
+    // wait for its partial results (a no-op after a plain launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t hq = (size_t)blockIdx.y * Hq + blockIdx.x;
     const int j = threadIdx.x, nt = blockDim.x;
     const int warp = j >> 5, lane = j & 31, nw = (nt + 31) >> 5;
@@ -324,7 +327,10 @@ w4a8_status launch_chunks(const uint16_t *q, const uint16_t *k, const uint16_t *
     return w4a8_host::launch_status();
 }
 
-int nsplits(int Lmax) { return (Lmax + C - 1) / C; }
+// chunks per sequence: 64 tokens on the tensor-core kernel (D 128, 256),
+// 128 on this file's kernel (D 64)
+int chunk_tokens(int D) { return (D == 128 || D == 256) ? w4a8_host::attention_tc_chunk() : C; }
+int nsplits(int D, int Lmax) { return (Lmax + chunk_tokens(D) - 1) / chunk_tokens(D); }
 
 }  // namespace
 
@@ -332,11 +338,11 @@ namespace w4a8_host {
 
 bool attention_shape_ok(int B, int Hq, int Hkv, int D, int Lmax) {
     return B >= 1 && Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0 && Hq / Hkv <= GMAX && (D == 64 || D == 128 || D == 256) &&
-           Lmax >= 1 && nsplits(Lmax) <= MAXS;
+           Lmax >= 1 && Lmax <= 131072 && nsplits(D, Lmax) <= MAXS;
 }
 
 size_t attention_workspace_bytes(int B, int Hq, int D, int Lmax) {
-    const int ns = nsplits(Lmax);
+    const int ns = nsplits(D, Lmax);
     if (ns == 1) return 0;
     const size_t o = (size_t)B * Hq * ns * D * 4;
     return ((o + 255) & ~(size_t)255) + (size_t)B * Hq * ns * 2 * 4;
@@ -345,7 +351,7 @@ size_t attention_workspace_bytes(int B, int Hq, int D, int Lmax) {
 w4a8_status launch_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *lens, int B, int Hq,
                              int Hkv, int D, int Lmax, uint16_t *out, void *workspace, size_t workspace_bytes,
                              cudaStream_t stream) {
-    const int ns = nsplits(Lmax);
+    const int ns = nsplits(D, Lmax);
     float *ws_o = nullptr, *ws_ml = nullptr;
     if (ns > 1) {
         const size_t need = attention_workspace_bytes(B, Hq, D, Lmax);
@@ -357,6 +363,26 @@ w4a8_status launch_attention(const uint16_t *q, const uint16_t *k, const uint16_
     const int G = Hq / Hkv;
     const int gp = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
     w4a8_status st = W4A8_ERR_UNSUPPORTED;
+    if (attention_tc_supported(D, Hq, Hkv)) {
+        // head dimensions 128 and 256: both contractions on the tensor cores
+        st = launch_attention_tc(q, k, v, lens, B, Hq, Hkv, D, Lmax, ns, out, ws_o, ws_ml, stream);
+        if (st != W4A8_OK || ns == 1) return st;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)Hq, (unsigned)B);
+        cfg.blockDim = dim3((unsigned)(D / 2), 1, 1);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, attn_combine_kernel, (const float *)ws_o, (const float *)ws_ml, Hq, D, ns, out) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return W4A8_ERR_CUDA;
+        }
+        return launch_status();
+    }
 #define W4A8_ATTN_CASE(DD, GG)                                                                                    \
     if (D == DD && gp == GG) st = launch_chunks<DD, GG>(q, k, v, lens, B, Hq, Hkv, Lmax, ns, out, ws_o, ws_ml, stream);
     W4A8_ATTN_CASE(64, 1) W4A8_ATTN_CASE(64, 2) W4A8_ATTN_CASE(64, 4) W4A8_ATTN_CASE(64, 8) W4A8_ATTN_CASE(64, 16)

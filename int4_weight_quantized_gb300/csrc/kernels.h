@@ -87,6 +87,14 @@ w4a8_status launch_linear_q8(const int8_t *codes, const float *sx, const void *p
 // Decode attention over an fp16 KV cache (attention.cu).
 bool attention_shape_ok(int B, int Hq, int Hkv, int D, int Lmax);
 size_t attention_workspace_bytes(int B, int Hq, int D, int Lmax);
+// tensor-core chunk kernel (attention_tc.cu): head dimension 128 or 256, up
+// to 16 query heads per KV head, 64-token chunks; same chunk outputs as
+// attention.cu's
+bool attention_tc_supported(int D, int Hq, int Hkv);
+int attention_tc_chunk();     // cached tokens per chunk of the tensor-core kernel
+w4a8_status launch_attention_tc(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *lens, int B,
+                                int Hq, int Hkv, int D, int Lmax, int nsplit, uint16_t *out, float *ws_o, float *ws_ml,
+                                cudaStream_t stream);
 w4a8_status launch_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *lens, int B, int Hq,
                              int Hkv, int D, int Lmax, uint16_t *out, void *workspace, size_t workspace_bytes,
                              cudaStream_t stream);

@@ -86,6 +86,32 @@ __device__ __forceinline__ void tmem_dealloc_512(uint32_t base) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(base) : "memory");
 }
 
+// `ncols` tensor-memory columns (a power of two, 32..512) for this CTA
+// (whole warp), so several CTAs can share an SM; base written to `dst`.
+__device__ __forceinline__ void tmem_alloc_cols(uint32_t dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_cols(uint32_t base, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols) : "memory");
+}
+
+// Shared-memory matrix descriptor for an MN-major operand with the 128-byte
+// swizzle, as a TMA box of 64 elements x rows lands it: each 128-byte row
+// holds 64 consecutive MN elements of one K index; `mn_stride` bytes
+// separate consecutive 64-element groups along MN, 8-row groups along K are
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t mn_stride) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;   // leading byte offset: next 64 along MN
+    d |= (uint64_t)(1024 >> 4) << 32;                    // stride byte offset: next 8 along K
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // N consecutive 32-bit columns of this thread's TMEM lane (warp-collective).

@@ -144,7 +144,8 @@ def test_new_entry_points_reject_bad_arguments(L):
 def test_new_workspace_sizes(L):
     """Workspace queries are pure host arithmetic: the fused decode routes
     need none; the unfused gated route holds the 2N-row intermediate; the
-    attention combine needs space only beyond one 128-token chunk."""
+    attention combine needs space only beyond one chunk (64 tokens for head
+    dimensions 128 and 256, 128 tokens for 64)."""
     L.w4a8_gated_workspace_bytes.restype = ctypes.c_size_t
     L.w4a8_linear_q8_workspace_bytes.restype = ctypes.c_size_t
     L.w4a8_decode_attention_workspace_bytes.restype = ctypes.c_size_t
@@ -152,10 +153,15 @@ def test_new_workspace_sizes(L):
     assert L.w4a8_gated_workspace_bytes(64, 128, 256) >= 64 * 256 * 2
     assert L.w4a8_linear_q8_workspace_bytes(1, 8192, 2048) == 0
     assert L.w4a8_linear_q8_workspace_bytes(64, 128, 256) == L.w4a8_workspace_bytes(64, 128, 256, 2)
-    assert L.w4a8_decode_attention_workspace_bytes(4, 8, 1, 256, 128) == 0
-    nb = L.w4a8_decode_attention_workspace_bytes(4, 8, 1, 256, 129)
+    assert L.w4a8_decode_attention_workspace_bytes(4, 8, 1, 256, 64) == 0
+    nb = L.w4a8_decode_attention_workspace_bytes(4, 8, 1, 256, 65)
     assert nb >= 4 * 8 * 2 * 256 * 4 + 4 * 8 * 2 * 2 * 4
+    assert L.w4a8_decode_attention_workspace_bytes(4, 8, 1, 256, 640) >= 4 * 8 * 10 * 256 * 4 + 4 * 8 * 10 * 2 * 4
+    assert L.w4a8_decode_attention_workspace_bytes(4, 8, 1, 64, 128) == 0
+    assert L.w4a8_decode_attention_workspace_bytes(4, 8, 1, 64, 129) >= 4 * 8 * 2 * 64 * 4
     assert L.w4a8_decode_attention_workspace_bytes(4, 8, 3, 256, 129) == 0      # invalid: 8 % 3
+    assert L.w4a8_decode_attention_workspace_bytes(1, 8, 1, 256, 131072) > 0
+    assert L.w4a8_decode_attention_workspace_bytes(1, 8, 1, 256, 131073) == 0   # past the longest cache
     assert L.w4a8_prefill_splits(512, 8192, 2048) == 1
     assert L.w4a8_prefill_splits(16, 128, 1056) == 8      # K % 256 != 0: the 128 x 128-tile kernel
     assert L.w4a8_prefill_splits(100, 256, 4096) == 8     # 128-token tiles of the streaming kernel

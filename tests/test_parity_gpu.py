@@ -239,6 +239,16 @@ def test_rmsnorm_quant(w4, M, K, with_res):
     assert np.mean(yg == y_ref) > 0.95
     qg, sg = oracle.quantize_act(yg)
     assert np.array_equal(_np(codes), qg) and np.array_equal(_np(sx), sg)
+    # end to end against the oracle's own codes: every 32-block whose y equals
+    # the oracle's y has identical codes and scale; the few blocks holding a
+    # one-ulp difference of y stay within one code step
+    same_blk = np.all((yg == y_ref).reshape(M, K // 32, 32), axis=2)
+    cg = _np(codes).reshape(M, K // 32, 32)
+    cr = q_ref.reshape(M, K // 32, 32)
+    assert np.array_equal(cg[same_blk], cr[same_blk])
+    assert np.array_equal(_np(sx).view(np.uint32)[same_blk], s_ref.view(np.uint32)[same_blk])
+    assert np.mean(same_blk) > 0.5
+    assert np.all(np.abs(cg[~same_blk].astype(np.int32) - cr[~same_blk].astype(np.int32)) <= 1)
 
 
 # (M, N, K, same kernel as the fp16 linear): codes input always decodes with
