@@ -365,8 +365,9 @@ w4a8_status launch_attention(const uint16_t *q, const uint16_t *k, const uint16_
     w4a8_status st = W4A8_ERR_UNSUPPORTED;
     if (attention_tc_supported(D, Hq, Hkv)) {
         // head dimensions 128 and 256: both contractions on the tensor cores
-        st = launch_attention_tc(q, k, v, lens, B, Hq, Hkv, D, Lmax, ns, out, ws_o, ws_ml, stream);
-        if (st != W4A8_OK || ns == 1) return st;
+        bool merged = false;
+        st = launch_attention_tc(q, k, v, lens, B, Hq, Hkv, D, Lmax, ns, out, ws_o, ws_ml, stream, &merged);
+        if (st != W4A8_OK || ns == 1 || merged) return st;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)Hq, (unsigned)B);
         cfg.blockDim = dim3((unsigned)(D / 2), 1, 1);

@@ -94,7 +94,7 @@ bool attention_tc_supported(int D, int Hq, int Hkv);
 int attention_tc_chunk();     // cached tokens per chunk of the tensor-core kernel
 w4a8_status launch_attention_tc(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *lens, int B,
                                 int Hq, int Hkv, int D, int Lmax, int nsplit, uint16_t *out, float *ws_o, float *ws_ml,
-                                cudaStream_t stream);
+                                cudaStream_t stream, bool *merged);   // merged: no combine pass needed
 w4a8_status launch_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *lens, int B, int Hq,
                              int Hkv, int D, int Lmax, uint16_t *out, void *workspace, size_t workspace_bytes,
                              cudaStream_t stream);

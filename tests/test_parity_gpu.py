@@ -291,12 +291,17 @@ def test_rmsnorm_then_linear_q8(w4):
 # ---------------------------------------------------------- decode attention
 
 # (B, Hq, Hkv, D, Lmax, lens): the decoder layer's 8 query heads over one KV
-# head of 256 (5 chunks of 128), ragged lengths incl. 1 and a chunk edge, one
-# chunk (direct write, no combine), 16 heads per group with D=64, 3 KV heads,
+# head of 256 (10 chunks of 64 on the tensor cores, merged in one cluster),
+# ragged lengths incl. 1 and a chunk edge (clusters with empty chunks), 16
+# chunks (the largest cluster), one chunk (direct write), 16 heads per group
+# with D=64 (128-token chunks on CUDA cores, combine kernel), 3 KV heads,
 # group sizes 3 and 5 (not powers of two)
 ATTN_CASES = [(1, 8, 1, 256, 640, [640]), (3, 8, 1, 256, 200, [1, 129, 200]), (2, 4, 2, 128, 128, [128, 64]),
               (4, 16, 1, 64, 300, [300, 1, 257, 128]), (2, 6, 3, 128, 1000, [999, 500]),
-              (2, 6, 2, 256, 130, [130, 3]), (1, 5, 1, 64, 64, [64])]
+              (2, 6, 2, 256, 130, [130, 3]), (1, 5, 1, 64, 64, [64]),
+              # tensor-core kernel: more than 16 chunks (workspace and combine
+              # kernel instead of the cluster merge), and one chunk
+              (2, 8, 2, 128, 1500, [1500, 700]), (2, 8, 1, 256, 64, [64, 10])]
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,D,Lmax,lens", ATTN_CASES)
