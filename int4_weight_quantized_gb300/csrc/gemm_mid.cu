@@ -26,8 +26,9 @@
 //     pass) as the B operand, warp 2 the block scales s_w (64 blocks of each
 //     row per load) and s_x;
 //   - warp 1 issues tcgen05.mma (M = 128 rows, N = tokens, K = 16), two per
-//     32-block, each block into its own TMEM accumulator of N columns; four
-//     accumulator units of 128 columns cycle between it and the epilogue;
+//     32-block, each block into its own TMEM accumulator of N columns; the
+//     accumulator units (four of 128 columns, or two of 256 at 128 tokens)
+//     cycle between it and the epilogue;
 //   - warps 8 and up (8 of them at 128 tokens, 16 at 64) read each block's
 //     exact integer dots (tcgen05.ld) and apply
 //     acc += d * (s_w * s_x) in fp32 (pairs of tokens per instruction);
@@ -59,7 +60,6 @@ constexpr int SG = 16;            // 32-blocks per s_x load
 constexpr int SS = 3;             // s_x stages
 constexpr int SWG = 64;           // 32-blocks per s_w load (128 bytes of each row)
 constexpr int SWS = 2;            // s_w stages
-constexpr int UNITS = 4;          // TMEM accumulator units of 128 columns (all 512)
 constexpr int A_TILE = BM * KS * 2;            // 16 KB
 constexpr int W_TILE = BM * 128;               // 16 KB: 128 rows x 128 bytes (4 stages), 128-byte swizzle
 constexpr int SW_TILE = BM * SWG * 2;          // 16 KB: 128 rows x 64 fp16, 128-byte swizzle
@@ -74,7 +74,13 @@ struct Layout {
     static constexpr int XS = NT == 64 ? 6 : 4;
     static constexpr int XP = XS / 2;                      // activation stage pairs (one barrier each)
     static constexpr int SX_TILE = SG * NT * 4;            // 16 blocks x NT tokens fp32
-    static constexpr int UB = 128 / NT;                    // blocks per accumulator unit
+    // accumulator units handed between the MMA and the epilogue: UB blocks
+    // of NT columns each, NU of them in the 512 TMEM columns (at 128 tokens
+    // two blocks per unit, so the epilogue's per-unit waits, scale loads and
+    // arrivals are paid once per two blocks)
+    static constexpr int UB = NT == 128 ? 2 : 128 / NT;
+    static constexpr int UCOLS = UB * NT;
+    static constexpr int NU = 512 / UCOLS;
     // int4 -> fp16 expansion warps (one thread per weight row; 8 warps with
     // two threads per row measured no faster)
     static constexpr int CONVW = 4;
@@ -91,7 +97,7 @@ struct Layout {
     static constexpr int OFF_SX = OFF_SW + SWS * SW_TILE;
     static constexpr int OFF_BAR = OFF_SX + SS * SX_TILE;
     // wfull, wempty; pfull, pempty; xfull, xempty; sfull, sempty (s_x); swfull, swempty; accfull, accempty; final
-    static constexpr int NUM_BARS = 2 * WS + 2 * PS + 2 * XP + 2 * SS + 2 * SWS + 2 * UNITS + 1;
+    static constexpr int NUM_BARS = 2 * WS + 2 * PS + 2 * XP + 2 * SS + 2 * SWS + 2 * NU + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;     // + slack to align the base to 1024
     static_assert(128 * NT * 4 <= AS * A_TILE, "split-K partial tile must fit the A ring");
@@ -105,6 +111,7 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
     constexpr int WS = LY::WS;
     constexpr int XS = LY::XS, XP = LY::XP;
     constexpr int UB = LY::UB;
+    constexpr int UNITS = LY::NU;
     constexpr int EPI_WARPS = LY::EPI_WARPS;
     constexpr int HT = NT / (EPI_WARPS / 4);   // tokens per epilogue thread
     extern __shared__ uint8_t smem_raw[];
@@ -231,7 +238,7 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
                         break;
                     }
                     if (jj == 0) tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)((u % UNITS) * 128 + jj * NT);
+                    const uint32_t d = tmem + (uint32_t)((u % UNITS) * LY::UCOLS + jj * NT);
                     const uint64_t ao = (uint64_t)(((st % AS) * A_TILE + (j & 1) * 64) >> 4);
                     const uint64_t xo = (uint64_t)(((st % XS) * LY::X_TILE + (j & 1) * 64) >> 4);
                     tc_mma_f16(d, adesc0 + ao, xdesc0 + xo, idesc, 0u);
@@ -335,7 +342,7 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
             if (!warp_wait(&accfull[u % UNITS], (uint32_t)(u / UNITS) & 1u, a, misc + 1)) { ok = false; break; }
             tc_fence_after();
             const float *sxt = reinterpret_cast<const float *>(smem + LY::OFF_SX + (g % SS) * LY::SX_TILE);
-            const uint32_t tu = tbase + (uint32_t)((u % UNITS) * 128);
+            const uint32_t tu = tbase + (uint32_t)((u % UNITS) * LY::UCOLS);
             if constexpr (NT <= 64) {
                 // all UB blocks of the unit in one batch of loads (UB * HT columns)
                 uint32_t d[UB][HT];
@@ -353,28 +360,32 @@ gemm_mid_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
                     scale_acc<HT, DEBUG>(acc, d[j], sw, sxt + (bl % SG) * NT + t0, n, m0 + t0, b0 + bl, a);
                 }
             } else {
-                // one block of 128 tokens: this thread's HT columns in chunks
-                // of 16, the next chunk's load in flight while the current one
-                // is scaled (tcgen05.wait::ld waits for all of a thread's
-                // loads, so the buffers alternate); the accumulator unit is
-                // released as soon as its last chunk has landed
-                constexpr int CH = HT / 16;
-                const float sw = __half2float(__ushort_as_half((uint16_t)(swu[0] & 0xffffu)));
-                const float *sxp = sxt + (bu % SG) * NT + t0;
+                // UB blocks of 128 tokens: this thread's HT columns of each in
+                // chunks of 16, the next chunk's load in flight while the
+                // current one is scaled (tcgen05.wait::ld waits for all of a
+                // thread's loads, so the buffers alternate); the accumulator
+                // unit is released as soon as its last chunk has landed
+                constexpr int CHB = HT / 16;             // chunks per block
+                constexpr int CH = UB * CHB;
                 const int mb = m0 + t0;
                 uint32_t dbuf[2][16];
                 tmem_ld_cols<16>(tu, dbuf[0]);
 #pragma unroll
                 for (int c = 0; c < CH; ++c) {
+                    const int j = c / CHB, cc = c % CHB;
                     tmem_ld_wait();
                     if (c + 1 < CH) {
-                        tmem_ld_cols<16>(tu + (uint32_t)(16 * (c + 1)), dbuf[(c + 1) & 1]);
+                        const int j1 = (c + 1) / CHB, cc1 = (c + 1) % CHB;
+                        tmem_ld_cols<16>(tu + (uint32_t)(j1 * NT + 16 * cc1), dbuf[(c + 1) & 1]);
                     } else {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&accempty[u % UNITS]);
                     }
-                    scale_acc<16, DEBUG>(acc + 8 * c, dbuf[c & 1], sw, sxp + 16 * c, n, mb + 16 * c, b0 + bu, a);
+                    const uint32_t pr = swu[j >> 1];
+                    const float sw = __half2float(__ushort_as_half((uint16_t)((j & 1) ? (pr >> 16) : (pr & 0xffffu))));
+                    scale_acc<16, DEBUG>(acc + 8 * cc, dbuf[c & 1], sw, sxt + ((bu + j) % SG) * NT + t0 + 16 * cc, n,
+                                         mb + 16 * cc, b0 + bu + j, a);
                 }
             }
             const int bl_last = bu + UB - 1;
