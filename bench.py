@@ -299,9 +299,10 @@ def main():
     # ---- end to end through the C entry point with pinned host buffers
     # Every step copies the step's inputs from pinned host memory, runs the
     # cps calls of w4a8_linear (the plain C entry point) and reads all outputs
-    # back, inside the timed region.  "graph": the calls are captured once
-    # into a CUDA graph, as a decode loop runs them; "eager": one Python call
-    # per linear (host-bound: ctypes and launch overhead per call).
+    # back, inside the timed region.  "graph": the step (input copy, the
+    # calls, output copy) is captured once into a CUDA graph and replayed, as
+    # a decode loop runs it; "eager": the copies and one Python call per
+    # linear (host-bound: ctypes and launch overhead per call).
     e2e_steps = max(3, min(args.steps, 50))
     xh = torch.empty((cps, lin.M, lin.K), dtype=torch.float16).pin_memory()
     xh.copy_(xs.cpu().expand(cps, lin.M, lin.K))
@@ -322,11 +323,17 @@ def main():
         e2e_step(e2e_calls)
         ge = torch.cuda.CUDAGraph()
         with torch.cuda.graph(ge, stream=stream):
+            xd.copy_(xh, non_blocking=True)
             e2e_calls()
-        e2e_step(ge.replay)
+            yh.copy_(yd, non_blocking=True)
+
+        def graph_step():
+            ge.replay()
+            stream.synchronize()
+        graph_step()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
-            e2e_step(ge.replay)
+            graph_step()
         e2e_graph_s = time.perf_counter() - t0
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
@@ -334,8 +341,8 @@ def main():
         e2e_eager_s = time.perf_counter() - t0
     e2e = {"value": ws * bytes_step * e2e_steps / e2e_graph_s / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": yh.numel() * 2, "steps": e2e_steps,
-           "note": "host wall clock per step: pinned x -> device, CUDA graph of the step's w4a8_linear calls, "
-                   "all y -> pinned host, synchronize",
+           "note": "host wall clock per step: one CUDA graph of the step (pinned x -> device copy, the step's "
+                   "w4a8_linear calls, all y -> pinned host copy), synchronize",
            "eager_value": ws * bytes_step * e2e_steps / e2e_eager_s / 1e9,
            "eager_note": "same step with one Python/ctypes w4a8_linear call per linear (host-bound)"}
 
