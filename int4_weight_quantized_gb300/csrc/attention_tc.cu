@@ -337,11 +337,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             wts[16 * 16 + h] = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
         }
         __syncthreads();
-        for (int idx = s * THREADS + threadIdx.x; idx < G * D; idx += S * THREADS) {
-            const int h = idx / D;
-            float o = 0.0f;
-            for (int z = 0; z < S; ++z) o = fmaf(ld_dsmem_f32(dsmem_addr(op_a + (uint32_t)(idx * 4), (uint32_t)z)), wts[h * 16 + z], o);
-            out[(hq0 + h) * D + idx % D] = __half_as_ushort(__float2half_rn(o * wts[16 * 16 + h]));
+        // four consecutive elements per thread: one 16-byte remote load per
+        // CTA of the cluster, all in flight together, summed in split order
+        for (int i4 = s * THREADS + threadIdx.x; i4 < G * D / 4; i4 += S * THREADS) {
+            const int idx = 4 * i4, h = idx / D;
+            float4 vz[16];
+#pragma unroll
+            for (int z = 0; z < 16; ++z)
+                vz[z] = z < S ? ld_dsmem_f32x4(dsmem_addr(op_a + (uint32_t)(idx * 4), (uint32_t)z)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int z = 0; z < 16; ++z) {
+                if (z < S) {
+                    const float w = wts[h * 16 + z];
+                    o.x = fmaf(vz[z].x, w, o.x);
+                    o.y = fmaf(vz[z].y, w, o.y);
+                    o.z = fmaf(vz[z].z, w, o.z);
+                    o.w = fmaf(vz[z].w, w, o.w);
+                }
+            }
+            const float inv = wts[16 * 16 + h];
+            const __half2 lo = __floats2half2_rn(o.x * inv, o.y * inv), hi = __floats2half2_rn(o.z * inv, o.w * inv);
+            uint2 pk;
+            pk.x = *reinterpret_cast<const uint32_t *>(&lo);
+            pk.y = *reinterpret_cast<const uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(out + (hq0 + h) * D + idx % D) = pk;
         }
         cluster_sync_all();   // no CTA leaves while a peer may still read its partials
     }

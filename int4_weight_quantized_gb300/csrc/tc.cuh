@@ -167,6 +167,13 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
     return v;
 }
 
+// Four consecutive fp32 from distributed shared memory (16-byte aligned).
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
 // Eight int4 weights of one packed word (k = 8j .. 8j+7, stored as w + 8,
 // byte t holding k = 8j+2t low and 8j+2t+1 high) as eight exact fp16 values
 // in the order k0 k4 k1 k5 k2 k6 k3 k7.  0x6400 | u is the fp16 value
