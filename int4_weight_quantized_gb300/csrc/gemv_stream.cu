@@ -39,8 +39,10 @@ using namespace w4a8;
 // When a lane holds few activation-code words in registers (tokens x code
 // slices x weight rows per output <= 2), registers are capped so that three
 // launches' CTAs fit on an SM at once: each CTA's weight copies are then
-// issued two launches before its rows are needed.  (More consumer warps do
-// not help: the work after the dependency wait is issue-bound.)
+// issued two launches before its rows are needed.  Heavier footprints keep
+// their registers (capping them for two CTAs per SM measured slower: the
+// rows lose their loads in flight).  (More consumer warps do not help: the
+// work after the dependency wait is issue-bound.)
 constexpr bool light_cfg(int MT, int BPL, int NV) { return MT * (BPL > 0 ? BPL : 1) * NV <= 2; }
 template <int MT, int BPL, int NV>
 struct Warps {
@@ -88,7 +90,9 @@ struct Layout {
     size_t ring, act_codes, act_sx, act_cb, part, bars, total;
 };
 
-__host__ __device__ inline Layout layout(int MT, int nb, size_t stage_bytes, int nslots) {
+constexpr int PART_FLOATS = 16;    // >= the partial sums a lane holds per pass (RG * MT * NV, rounded up)
+
+__host__ __device__ inline Layout layout(int MT, int nb, size_t stage_bytes, int nslots, int kg) {
     Layout L;
     size_t o = 0;
     L.ring = o;
@@ -99,8 +103,9 @@ __host__ __device__ inline Layout layout(int MT, int nb, size_t stage_bytes, int
     o += (size_t)MT * nb * 4;
     L.act_cb = o;
     o += (size_t)MT * nb * 4;
-    L.part = o;
     o = (o + 15) & ~(size_t)15;
+    L.part = o;                     // K-group partial sums: [2 passes][consumer warps][PART_FLOATS]
+    if (kg > 1) o += 2 * 8 * PART_FLOATS * 4;
     L.bars = o;
     o += 2 * STAGES * 8;
     L.total = o;
@@ -125,6 +130,11 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 
 template <int CW>
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory"); }
+
+// The warps of one row slot (ids 2.. are free: 0 is __syncthreads, 1 the consumers).
+__device__ __forceinline__ void slot_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 constexpr int pow2ceil(int v) { return v <= 1 ? 1 : 2 * pow2ceil((v + 1) / 2); }
@@ -164,16 +174,20 @@ __device__ __forceinline__ float warp_reduce_halving(float (&v)[P], int lane) {
 // branches fused into the fully connected operator.
 // Q8: the activations arrive already quantised (int8 codes and fp32 block
 // scales, e.g. from the RMS-normalisation operator) instead of as fp16 x.
-template <int MT, int BPL, bool DEBUG, bool GATED, bool Q8>
+// KG > 1 (codes in registers, one token): the K blocks form KG groups of 32
+// BPL blocks, and KG consumer warps share each row, one group each.
+template <int MT, int BPL, int KG, bool DEBUG, bool GATED, bool Q8>
 __global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<MT, BPL, GATED ? 2 : 1>::MIN_CTAS)
     gemv_stream_kernel(StreamArgs a) {
     static_assert(!(DEBUG && GATED) && !(DEBUG && Q8), "the debug instantiation is the plain linear");
     constexpr int NV = GATED ? 2 : 1;         // weight rows per output row
     constexpr int CWARPS = Warps<MT, BPL, NV>::CW;
     constexpr int RG = (8 / MT) < RG_MAX ? (8 / MT) : RG_MAX;
+    static_assert(CWARPS == 8, "the partial-sum region is sized for 8 consumer warps");
+    static_assert(KG == 1 || (BPL > 0 && CWARPS % KG == 0), "K groups need register codes and whole row slots");
     const int rgr = a.rg;
     extern __shared__ __align__(16) uint8_t smem[];
-    const Layout L = layout(MT, a.nb, a.stage_bytes, a.nslots);
+    const Layout L = layout(MT, a.nb, a.stage_bytes, a.nslots, KG);
     const int NS = a.nslots;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + NS;
@@ -236,67 +250,99 @@ __global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<
     int *cbs = reinterpret_cast<int *>(smem + L.act_cb);
     const int tid = threadIdx.x;
     {
+        // When all of x takes two rounds of the consumer threads, both
+        // rounds' loads are issued before either is quantised (one load
+        // latency instead of two); longer x keeps one load per round
+        // (batching more rounds measured slower there).
         const int items = MT * a.nb * 4;
-        for (int base = 0; base < items; base += CWARPS * 32) {
-            const int i = base + tid;
-            const bool act = i < items;
-            int m = 0, b = 0, t = 0;
-            uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-            if (act) {
-                m = i / (a.nb * 4);
-                const int rem = i - m * a.nb * 4;
-                b = rem >> 2;
-                t = rem & 3;
-                if (!Q8 && m < a.M) xv = *reinterpret_cast<const uint4 *>(a.x + (size_t)m * a.K + (size_t)b * kBlock + t * 8);
-            }
-            if constexpr (Q8) {
-                // 8 codes of this block: even k to one word, odd k to the other,
-                // as the quantiser below packs them; the block's code sum for
-                // the unsigned-weight offset comes from two dp4a with ones
-                uint2 cv = make_uint2(0u, 0u);
-                float sxv = 0.0f;
-                if (act) {
-                    // both loads in flight together: the scale does not wait for the code sums
-                    cv = *reinterpret_cast<const uint2 *>(a.xq + (size_t)m * a.K + (size_t)b * kBlock + t * 8);
-                    if (t == 0) sxv = a.xs[(size_t)m * a.nb + b];
-                }
-                int sum = __dp4a((int)cv.x, 0x01010101, __dp4a((int)cv.y, 0x01010101, 0));
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1, 4);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2, 4);
-                if (act) {
-                    uint32_t *cw = codes + ((size_t)m * a.nb + b) * 8;
-                    cw[2 * t] = __byte_perm(cv.x, cv.y, 0x6420);
-                    cw[2 * t + 1] = __byte_perm(cv.x, cv.y, 0x7531);
-                    if (t == 0) {
-                        sxs[m * a.nb + b] = sxv;
-                        cbs[m * a.nb + b] = kMagicBits - 8 * sum;
+        constexpr int XB = Warps<MT, BPL, NV>::LIGHT ? 1 : 2;
+        constexpr int STRIDE = CWARPS * 32;
+        const int xb = items <= XB * STRIDE ? XB : 1;
+        for (int base0 = 0; base0 < items; base0 += xb * STRIDE) {
+            uint4 xv[XB];
+            uint2 cv[XB];
+            float sxq[XB];
+#pragma unroll
+            for (int u = 0; u < XB; ++u) {
+                const int i = base0 + u * STRIDE + tid;
+                xv[u] = make_uint4(0u, 0u, 0u, 0u);
+                cv[u] = make_uint2(0u, 0u);
+                sxq[u] = 0.0f;
+                if (u < xb && i < items) {
+                    const int m = i / (a.nb * 4);
+                    const int rem = i - m * a.nb * 4;
+                    const int b = rem >> 2, t = rem & 3;
+                    if constexpr (Q8) {
+                        // codes and scale in flight together: the scale does not wait for the code sums
+                        cv[u] = *reinterpret_cast<const uint2 *>(a.xq + (size_t)m * a.K + (size_t)b * kBlock + t * 8);
+                        if (t == 0) sxq[u] = a.xs[(size_t)m * a.nb + b];
+                    } else if (m < a.M) {
+                        xv[u] = *reinterpret_cast<const uint4 *>(a.x + (size_t)m * a.K + (size_t)b * kBlock + t * 8);
                     }
                 }
-                continue;
             }
-            Quant8 r = quant8_group4(xv);
-            if (act) {
-                uint32_t *cw = codes + ((size_t)m * a.nb + b) * 8;
-                cw[2 * t] = pack_bytes4(r.q[0], r.q[2], r.q[4], r.q[6]);
-                cw[2 * t + 1] = pack_bytes4(r.q[1], r.q[3], r.q[5], r.q[7]);
-                if (t == 0) {
-                    sxs[m * a.nb + b] = r.s;
-                    cbs[m * a.nb + b] = kMagicBits - 8 * r.sum;
+#pragma unroll
+            for (int u = 0; u < XB; ++u) {
+                const int ib = base0 + u * STRIDE;
+                if (u >= xb || ib >= items) break;   // the same for every consumer thread
+                const int i = ib + tid;
+                const bool act = i < items;
+                int m = 0, b = 0, t = 0;
+                if (act) {
+                    m = i / (a.nb * 4);
+                    const int rem = i - m * a.nb * 4;
+                    b = rem >> 2;
+                    t = rem & 3;
+                }
+                if constexpr (Q8) {
+                    // 8 codes of this block: even k to one word, odd k to the
+                    // other, as the quantiser below packs them; the block's code
+                    // sum for the unsigned-weight offset comes from two dp4a with ones
+                    int sum = __dp4a((int)cv[u].x, 0x01010101, __dp4a((int)cv[u].y, 0x01010101, 0));
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1, 4);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 2, 4);
+                    if (act) {
+                        uint32_t *cw = codes + ((size_t)m * a.nb + b) * 8;
+                        cw[2 * t] = __byte_perm(cv[u].x, cv[u].y, 0x6420);
+                        cw[2 * t + 1] = __byte_perm(cv[u].x, cv[u].y, 0x7531);
+                        if (t == 0) {
+                            sxs[m * a.nb + b] = sxq[u];
+                            cbs[m * a.nb + b] = kMagicBits - 8 * sum;
+                        }
+                    }
+                } else {
+                    Quant8 r = quant8_group4(xv[u]);
+                    if (act) {
+                        uint32_t *cw = codes + ((size_t)m * a.nb + b) * 8;
+                        cw[2 * t] = pack_bytes4(r.q[0], r.q[2], r.q[4], r.q[6]);
+                        cw[2 * t + 1] = pack_bytes4(r.q[1], r.q[3], r.q[5], r.q[7]);
+                        if (t == 0) {
+                            sxs[m * a.nb + b] = r.s;
+                            cbs[m * a.nb + b] = kMagicBits - 8 * r.sum;
+                        }
+                    }
                 }
             }
         }
     }
     consumer_sync<CWARPS>();
 
-    // this lane's K blocks (lane + 32 j) and their activation codes, in registers
+    // Row slots: the KG warps w with equal w / KG compute the same rows, warp
+    // w over the K blocks of group w % KG (32 BPL consecutive blocks), and
+    // their partial sums meet in shared memory.  Warps past the last whole
+    // slot only take part in the chunk hand-offs.
+    const int kgi = warp % KG, slot = warp / KG;
+    constexpr int nslot = CWARPS / KG;
+    // this lane's K blocks (g0 + lane + 32 j) and their activation codes, in registers
     constexpr int BR = BPL > 0 ? BPL : 1;
+    const int g0 = kgi * 32 * BR;
     uint32_t qa[MT][BR][8];
     float sxr[MT][BR];
     int cbr[MT][BR];
     if constexpr (BPL > 0) {
 #pragma unroll
         for (int j = 0; j < BPL; ++j) {
-            const int b = lane + 32 * j;
+            const int b = g0 + lane + 32 * j;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 if (b < a.nb) {
@@ -317,12 +363,23 @@ __global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<
     }
 
     const bool reuse = nchunks > NS;         // ring slots are refilled: release them
+    // A warp whose wait ran out leaves at once when it computes rows alone;
+    // in a slot of several warps it stops waiting but keeps meeting its
+    // partners at every slot barrier, so none of them waits forever (the
+    // status word already holds the error).
+    bool alive = true;
+    int pp = 0;                              // pass parity: which half of the partial-sum region
     for (int c = 0; c < nchunks; ++c) {
         const int s = c % NS;
         const uint32_t ph = (uint32_t)(c / NS) & 1u;
-        bool ok = mbar_wait_bounded(&full[s], ph, a.budget, a.status);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) return;
+        if (alive) {
+            bool ok = mbar_wait_bounded(&full[s], ph, a.budget, a.status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if constexpr (KG == 1) return;
+                alive = false;
+            }
+        }
         const uint8_t *wst = smem + L.ring + (size_t)s * a.stage_bytes;
         const uint16_t *sst = reinterpret_cast<const uint16_t *>(wst + NV * w_stage);
         const int rows = min(a.cr, nrows - c * a.cr);
@@ -331,10 +388,10 @@ __global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<
         for (int base = 0; base < rows;) {
             // rows per warp in this pass: at most rgr, and no more than the
             // remaining rows need, so the last pass spreads over all warps
-            const int rgp = min(rgr, (rows - base + CWARPS - 1) / CWARPS);
-            const int rb = base + warp * rgp;
-            base += CWARPS * rgp;
-            if (rb >= rows) continue;
+            const int rgp = min(rgr, (rows - base + nslot - 1) / nslot);
+            const int rb = base + slot * rgp;
+            base += nslot * rgp;
+            if (slot >= nslot || rb >= rows) continue;
             // partial sums of this lane: value (g * MT + m) * NV + br is output
             // row rb + g, token m, branch br (0 gate or plain, 1 up)
             constexpr int NVAL = RG * MT * NV;
@@ -387,7 +444,7 @@ __global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<
                     if constexpr (BPL > 0) {
     #pragma unroll
                         for (int j = 0; j < BPL; ++j) {
-                            const int b = lane + 32 * j;
+                            const int b = g0 + lane + 32 * j;
                             const bool bvalid = b < a.nb;          // codes of such blocks are zero
                             const int bc = bvalid ? b : a.nb - 1;
                             const uint16_t swh = a.sw_bulk ? srow[bc] : __ldg(sglob + bc);
@@ -427,7 +484,17 @@ __global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<
             else rows_pass(std::false_type{});
             float t = warp_reduce_halving<P>(v, lane);
             constexpr int SH = 5 - ilog2(P);             // lanes per value after the reduction: 1 << SH
+            static_assert(P <= PART_FLOATS, "partial-sum region too small");
             const int vi = lane >> SH;
+            if constexpr (KG > 1) {
+                // the slot's partial sums, added in K-group order by its first warp
+                float *part = reinterpret_cast<float *>(smem + L.part) + (size_t)pp * CWARPS * PART_FLOATS;
+                if ((lane & ((1 << SH) - 1)) == 0) part[warp * PART_FLOATS + vi] = t;
+                slot_sync(2 + slot, KG * 32);
+                pp ^= 1;
+                if (kgi != 0 || !alive) continue;
+                for (int g2 = 1; g2 < KG; ++g2) t += part[(slot * KG + g2) * PART_FLOATS + vi];
+            }
             if constexpr (GATED) t = gate_act(a.act, t) * __shfl_xor_sync(0xffffffffu, t, 1 << SH);
             const int br = vi % NV, g = (vi / NV) / MT, m = (vi / NV) % MT;
             if ((lane & ((1 << SH) - 1)) == 0 && vi < NVAL && br == 0 && g < rgp && rb + g < rows && m < a.M)
@@ -441,7 +508,7 @@ __global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<
 }
 
 struct Plan {
-    int MT, BPL, R, cr, rg, sw_bulk, nslots;
+    int MT, BPL, KG, R, cr, rg, sw_bulk, nslots;
     size_t stage_bytes, smem;
     int grid;
     bool ok;
@@ -449,19 +516,41 @@ struct Plan {
 
 constexpr int kSMs = 152;
 
+// Where the activation codes live: BPL blocks per lane (1, 2, 4 or 8) in
+// each of KG K groups of 32 BPL blocks (KG warps per row slot).  Several
+// tokens keep one group: BPL = K/32 slices rounded up to a power of two
+// while tokens x BPL <= 8, else the codes stay in shared memory (BPL = 0).
+// One token with rows of more than 4 slices (K > 4096) takes 4 slices per
+// lane in 2 or 4 groups (up to K = 16384): the codes of 8 slices, or codes
+// read from shared memory, measured slower.
+void pick_codes(int MT, int nb, int &bpl, int &kg) {
+    const int need = (nb + 31) / 32;
+    int b = 1;
+    while (b < need) b *= 2;
+    kg = 1;
+    bpl = (b <= 8 && MT * b <= 8) ? b : 0;
+    if (MT == 1 && b > 4 && need <= 16) {
+        bpl = 4;
+        kg = need <= 8 ? 2 : 4;
+    }
+}
+
 // Launch plan: each of (up to) 152 CTAs owns R consecutive rows, streamed in
 // chunks of cr rows through an nslots-deep ring.  Chunks aim at about a
 // quarter of the CTA's bytes (at least 64 KB, so a CTA of up to 64 KB is one
-// chunk).  When the ring does not fit,
-// fewer slots are tried before smaller chunks (down to two slots), first
-// within the co-resident budget, then with one CTA per SM.
+// chunk).  A CTA that needs several fills wants at least three slots, so a
+// slot is always being filled while another is read; the ring is sized, in
+// this order, for co-resident CTAs (the lightest register footprints: the
+// next launches' copies then start during this one) with three slots, for
+// one CTA per SM with three slots, and the same with two.  Within each
+// budget the largest chunk wins, but not one below a row per row slot while
+// another budget remains.
 Plan make_plan(int M, int N, int K, int nv = 1) {
     // nv = weight rows per output row (2 for the gated kernel)
     Plan p{};
     const int nb = K / 32;
     p.MT = M < 8 ? M : 8;
-    p.BPL = (nb + 31) / 32;
-    if (!((p.BPL == 1 || p.BPL == 2 || p.BPL == 4 || p.BPL == 8) && p.MT * p.BPL <= 8)) p.BPL = 0;
+    pick_codes(p.MT, nb, p.BPL, p.KG);
     const size_t row_bytes = (size_t)nv * K / 2;
     p.sw_bulk = (nb % 8) == 0;
     p.R = (N + kSMs - 1) / kSMs;
@@ -472,40 +561,49 @@ Plan make_plan(int M, int N, int K, int nv = 1) {
     int cr0 = (int)(target / row_bytes);
     if (cr0 < 1) cr0 = 1;
     if (cr0 > p.R) cr0 = p.R;
-    auto fit = [&](int cr, size_t limit) {
+    auto fit = [&](int cr, size_t limit, int min_slots) {
         p.cr = cr;
         p.stage_bytes = ((size_t)cr * row_bytes + (p.sw_bulk ? (size_t)nv * cr * nb * 2 : 0) + 15) & ~(size_t)15;
         const int nch = (p.R + cr - 1) / cr;
         p.nslots = nch < STAGES ? nch : STAGES;
+        const int floor_slots = nch < min_slots ? nch : min_slots;
         for (;;) {
-            p.smem = layout(p.MT, nb, p.stage_bytes, p.nslots).total;
-            if (p.smem <= limit || p.nslots <= 2) break;
+            p.smem = layout(p.MT, nb, p.stage_bytes, p.nslots, p.KG).total;
+            if (p.smem <= limit || p.nslots <= floor_slots) break;
             --p.nslots;
         }
         return p.smem <= limit;
     };
-    const int cw = Warps<1, 1, 1>::CW;
+    const int row_slots = Warps<1, 1, 1>::CW / p.KG;
+    const bool share = light_cfg(p.MT, p.BPL, nv);
+    struct Budget {
+        size_t limit;
+        int min_slots;
+    };
+    const Budget budgets[] = {{(size_t)SMEM_COTENANT, 3}, {(size_t)SMEM_ALONE, 3}, {(size_t)SMEM_COTENANT, 2},
+                              {(size_t)SMEM_ALONE, 2}};
     bool ok = false;
-    for (size_t limit : {(size_t)SMEM_COTENANT, (size_t)SMEM_ALONE}) {
-        for (int cr = cr0; cr >= 1 && !ok; cr = (cr == 1 ? 0 : (cr + 1) / 2)) {
-            ok = fit(cr, limit);
-            if (ok && cr < cw && cr < cr0 && limit == SMEM_COTENANT) ok = false;   // try one CTA per SM first
+    for (const Budget &b : budgets) {
+        if (b.limit == (size_t)SMEM_COTENANT && !share) continue;
+        for (int cr = cr0; cr >= 1 && !ok; --cr) {
+            ok = fit(cr, b.limit, b.min_slots);
+            if (ok && cr < row_slots && cr < cr0) ok = false;
         }
         if (ok) break;
     }
-    if (!ok) {   // last resort: the smallest ring that fits alone
-        for (int cr = cr0; cr >= 1 && !ok; cr = (cr == 1 ? 0 : (cr + 1) / 2)) ok = fit(cr, SMEM_ALONE);
+    if (!ok) {   // last resort: the largest chunk that fits alone
+        for (int cr = cr0; cr >= 1 && !ok; --cr) ok = fit(cr, SMEM_ALONE, 2);
     }
     // rows per warp and pass: the kernel spreads each pass's rows over all
-    // consumer warps (at most this many per warp)
+    // row slots (at most this many per slot)
     p.rg = (8 / p.MT) < RG_MAX ? (8 / p.MT) : RG_MAX;
     p.ok = ok;
     return p;
 }
 
-template <int MT, int BPL, bool DEBUG, bool GATED, bool Q8>
+template <int MT, int BPL, int KG, bool DEBUG, bool GATED, bool Q8>
 w4a8_status launch_t(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
-    auto kern = gemv_stream_kernel<MT, BPL, DEBUG, GATED, Q8>;
+    auto kern = gemv_stream_kernel<MT, BPL, KG, DEBUG, GATED, Q8>;
     static std::atomic<int> attr_done[w4a8_host::kDeviceSlots];
     const w4a8_status ast = w4a8_host::ensure_smem_limit(kern, SMEM_ALONE, attr_done);
     if (ast != W4A8_OK) return ast;
@@ -528,30 +626,33 @@ w4a8_status launch_t(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
 
 template <bool DEBUG, bool GATED, bool Q8>
 w4a8_status dispatch(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
+    if (p.KG == 2 && p.MT == 1 && p.BPL == 4) return launch_t<1, 4, 2, DEBUG, GATED, Q8>(p, a, stream);
+    if (p.KG == 4 && p.MT == 1 && p.BPL == 4) return launch_t<1, 4, 4, DEBUG, GATED, Q8>(p, a, stream);
+    if (p.KG != 1) return W4A8_ERR_UNSUPPORTED;
     switch (p.MT * 16 + p.BPL) {
-        case 1 * 16 + 1: return launch_t<1, 1, DEBUG, GATED, Q8>(p, a, stream);
-        case 1 * 16 + 2: return launch_t<1, 2, DEBUG, GATED, Q8>(p, a, stream);
-        case 1 * 16 + 4: return launch_t<1, 4, DEBUG, GATED, Q8>(p, a, stream);
-        case 1 * 16 + 8: return launch_t<1, 8, DEBUG, GATED, Q8>(p, a, stream);
-        case 2 * 16 + 1: return launch_t<2, 1, DEBUG, GATED, Q8>(p, a, stream);
-        case 2 * 16 + 2: return launch_t<2, 2, DEBUG, GATED, Q8>(p, a, stream);
-        case 2 * 16 + 4: return launch_t<2, 4, DEBUG, GATED, Q8>(p, a, stream);
-        case 3 * 16 + 1: return launch_t<3, 1, DEBUG, GATED, Q8>(p, a, stream);
-        case 3 * 16 + 2: return launch_t<3, 2, DEBUG, GATED, Q8>(p, a, stream);
-        case 4 * 16 + 1: return launch_t<4, 1, DEBUG, GATED, Q8>(p, a, stream);
-        case 4 * 16 + 2: return launch_t<4, 2, DEBUG, GATED, Q8>(p, a, stream);
-        case 5 * 16 + 1: return launch_t<5, 1, DEBUG, GATED, Q8>(p, a, stream);
-        case 6 * 16 + 1: return launch_t<6, 1, DEBUG, GATED, Q8>(p, a, stream);
-        case 7 * 16 + 1: return launch_t<7, 1, DEBUG, GATED, Q8>(p, a, stream);
-        case 8 * 16 + 1: return launch_t<8, 1, DEBUG, GATED, Q8>(p, a, stream);
-        case 1 * 16 + 0: return launch_t<1, 0, DEBUG, GATED, Q8>(p, a, stream);
-        case 2 * 16 + 0: return launch_t<2, 0, DEBUG, GATED, Q8>(p, a, stream);
-        case 3 * 16 + 0: return launch_t<3, 0, DEBUG, GATED, Q8>(p, a, stream);
-        case 4 * 16 + 0: return launch_t<4, 0, DEBUG, GATED, Q8>(p, a, stream);
-        case 5 * 16 + 0: return launch_t<5, 0, DEBUG, GATED, Q8>(p, a, stream);
-        case 6 * 16 + 0: return launch_t<6, 0, DEBUG, GATED, Q8>(p, a, stream);
-        case 7 * 16 + 0: return launch_t<7, 0, DEBUG, GATED, Q8>(p, a, stream);
-        case 8 * 16 + 0: return launch_t<8, 0, DEBUG, GATED, Q8>(p, a, stream);
+        case 1 * 16 + 1: return launch_t<1, 1, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 1 * 16 + 2: return launch_t<1, 2, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 1 * 16 + 4: return launch_t<1, 4, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 1 * 16 + 8: return launch_t<1, 8, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 2 * 16 + 1: return launch_t<2, 1, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 2 * 16 + 2: return launch_t<2, 2, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 2 * 16 + 4: return launch_t<2, 4, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 3 * 16 + 1: return launch_t<3, 1, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 3 * 16 + 2: return launch_t<3, 2, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 4 * 16 + 1: return launch_t<4, 1, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 4 * 16 + 2: return launch_t<4, 2, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 5 * 16 + 1: return launch_t<5, 1, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 6 * 16 + 1: return launch_t<6, 1, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 7 * 16 + 1: return launch_t<7, 1, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 8 * 16 + 1: return launch_t<8, 1, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 1 * 16 + 0: return launch_t<1, 0, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 2 * 16 + 0: return launch_t<2, 0, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 3 * 16 + 0: return launch_t<3, 0, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 4 * 16 + 0: return launch_t<4, 0, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 5 * 16 + 0: return launch_t<5, 0, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 6 * 16 + 0: return launch_t<6, 0, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 7 * 16 + 0: return launch_t<7, 0, 1, DEBUG, GATED, Q8>(p, a, stream);
+        case 8 * 16 + 0: return launch_t<8, 0, 1, DEBUG, GATED, Q8>(p, a, stream);
         default: return W4A8_ERR_UNSUPPORTED;
     }
 }

@@ -93,11 +93,14 @@ def test_quantizer_bit_exact(w4, M, K, scale, outliers):
 # ---------------------------------------------------------- block dots
 
 # decode kernels by shape: codes in registers (K/32 in 1, 2, 4 or 8 slices of
-# 32 blocks and tokens x slices <= 8), codes read from shared memory (one or two
-# tokens, any K; long rows make small chunks, and the longest need one CTA per
-# SM), and the cluster split-K kernel (3 to 8 tokens with long rows)
+# 32 blocks and tokens x slices <= 8), one token with rows of 5-16 slices in 2
+# or 4 K groups of 4 slices (ragged last groups: 193 and 448 blocks), codes
+# read from shared memory (two tokens with long rows; long rows make small
+# chunks, and the longest need one CTA per SM), and the cluster split-K kernel
+# (3 to 8 tokens with long rows)
 DOT_SHAPES = [(1, 1, 32), (1, 37, 96), (2, 100, 1024), (3, 64, 1056), (8, 129, 2048), (5, 257, 4096),
-              (1, 300, 3072), (2, 77, 14336), (1, 40, 14336), (1, 700, 14336), (1, 1500, 4096)]
+              (1, 300, 3072), (2, 77, 14336), (1, 40, 14336), (1, 700, 14336), (1, 1500, 4096),
+              (1, 130, 6176), (1, 2048, 8192)]
 
 
 @pytest.mark.parametrize("path", [1, 2])
@@ -172,7 +175,8 @@ def test_mid_path_split_counts(w4):
 # shared memory with one or two tokens); the others take the linear over 2N
 # rows and the element-wise pass
 GATED_SHAPES = [(1, 64, 64, True), (1, 300, 2048, True), (2, 96, 3072, True), (3, 130, 1024, True),
-                (8, 200, 256, True), (1, 1000, 4096, True), (5, 70, 4096, False), (9, 70, 512, False),
+                (8, 200, 256, True), (1, 1000, 4096, True), (1, 96, 8192, True), (5, 70, 4096, False),
+                (9, 70, 512, False),
                 (64, 128, 256, False), (200, 96, 320, False)]
 
 
@@ -254,7 +258,8 @@ def test_rmsnorm_quant(w4, M, K, with_res):
 # (M, N, K, same kernel as the fp16 linear): codes input always decodes with
 # the streaming kernel, while the fp16 linear takes the cluster split-K
 # kernel for 3-8 tokens with long rows, whose summation order differs
-Q8_SHAPES = [(1, 512, 2048, True), (2, 300, 3072, True), (5, 257, 4096, False), (8, 129, 2048, False),
+Q8_SHAPES = [(1, 512, 2048, True), (2, 300, 3072, True), (1, 200, 10240, True), (5, 257, 4096, False),
+             (8, 129, 2048, False),
              (9, 130, 512, True), (64, 96, 256, True), (200, 70, 320, True)]
 
 
