@@ -292,7 +292,7 @@ def main():
     achieved = lin.bytes / per_launch_s / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": traffic_for("gemv_stream_decode_ffn_up", gemv_files), "peak_source": peak_src,
-            "kernel": "gemv_stream_kernel<1,2,false,false,false>", "algorithmic_bytes_per_launch": lin.bytes,
+            "kernel": "gemv_stream_kernel<1,2,1,false,false,false>", "algorithmic_bytes_per_launch": lin.bytes,
             "launch_time_us": per_launch_s * 1e6,
             "note": "launch time = timed region / launches (every launch in the step is this kernel)"}
 
