@@ -70,10 +70,6 @@ struct Quant8 {
 // fl(127 / amax), with amax 0 mapped to 0 (every x of such a block is 0).
 __device__ __forceinline__ float act_recip(float amax) { return amax == 0.0f ? 0.0f : __fdiv_rn(127.0f, amax); }
 
-// Codes of one element by the definition, rint(fl(x / s)) clamped: the
-// fallback of the fast path below.
-static __device__ __noinline__ int act_code_exact(float x, float s) { return act_code(x, s); }
-
 // Quantise one block held by 4 consecutive lanes (lane % 4 == t), 8 fp16
 // values each.  Every lane of the warp must call this together (full-mask
 // shuffles of width 4); lanes with no data pass zeros.
@@ -87,7 +83,9 @@ static __device__ __noinline__ int act_code_exact(float x, float s) { return act
 // When t is at least 2^-14 away from every half-integer, no rounding
 // boundary lies between t and fl(x/s), so rint(t) = rint(fl(x/s)); the
 // elements closer than that to a boundary (one in several thousand for
-// random data, and every exact tie) are divided exactly instead.  In both
+// random data, and every exact tie) are divided exactly instead, each on
+// its own and inline (a called routine with a stack frame cost ~0.6 us per
+// launch whenever one element of the activations needed it).  In both
 // cases |code| <= 127, so the clamp never changes a value.
 __device__ __forceinline__ Quant8 quant8_group4(uint4 xv) {
     const __half2 *h = reinterpret_cast<const __half2 *>(&xv);
@@ -106,28 +104,22 @@ __device__ __forceinline__ Quant8 quant8_group4(uint4 xv) {
     Quant8 r;
     r.s = act_scale(a);
     const float rc = act_recip(a);
-    bool near = false;
-    float c[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float t = f[i] * rc;
-        c[i] = rintf(t);
-        near |= fabsf(t - c[i]) > 0.5f - 0x1p-14f;
-    }
+    unsigned near = 0u;
     int sum = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        r.q[i] = (int)c[i];
-        sum += r.q[i];
+        const float t = f[i] * rc;
+        const float c = rintf(t);
+        if (fabsf(t - c) > 0.5f - 0x1p-14f) near |= 1u << i;
+        r.q[i] = (int)c;
     }
     if (near) {
-        sum = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            r.q[i] = act_code_exact(f[i], r.s);
-            sum += r.q[i];
-        }
+        for (int i = 0; i < 8; ++i)
+            if (near & (1u << i)) r.q[i] = act_code(f[i], r.s);
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum += r.q[i];
     sum += __shfl_xor_sync(0xffffffffu, sum, 1, 4);
     sum += __shfl_xor_sync(0xffffffffu, sum, 2, 4);
     r.sum = sum;

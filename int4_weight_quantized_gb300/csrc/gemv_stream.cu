@@ -211,6 +211,19 @@ __global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<
     if (warp == CWARPS) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            // The activations into L2 ahead of the dependency wait: L2 is the
+            // point of coherence, so lines the previous kernel writes later
+            // are updated there, and the loads after the wait (which do not
+            // hit this SM's L1 before it) see its results.  When x comes from
+            // a host copy or an older kernel this takes an HBM round trip off
+            // the post-wait chain.
+            if constexpr (!Q8) {
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.x), "r"((uint32_t)(a.M * a.K * 2))
+                             : "memory");
+            } else {
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.xq), "r"((uint32_t)(a.M * a.K))
+                             : "memory");
+            }
             const uint64_t pol = policy_evict_first();
             int issued = 0;
             for (int c = 0; c < nchunks; ++c) {
