@@ -113,14 +113,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int G = Hq / Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int L = lens[b];
-    L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
     const int t0 = s * C;
-    const int n = max(0, min(C, L - t0));
     const size_t hq0 = (size_t)b * Hq + (size_t)g * G;
-    // q and the output buffers may come from the previous kernel on the stream
+    // The chunk's K and V boxes into L2 ahead of the dependency wait.  L2 is
+    // the point of coherence, so rows the previous kernel writes later are
+    // updated there; the length read here only decides whether to fetch.
+    if (threadIdx.x == 0) {
+        const int Lh = lens[b];
+        if (Lh > t0 && t0 < Lmax) {
+            const int row0 = (b * Hkv + g) * Lmax + t0;
+            for (int c = 0; c < KT; ++c) {
+                tma_prefetch_2d(&tm_k, c * 64, row0);
+                tma_prefetch_2d(&tm_v, c * 64, row0);
+            }
+        }
+    }
+    // q, the lengths and the output buffers may come from the previous kernel
+    // on the stream
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    int L = lens[b];
+    L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
+    const int n = max(0, min(C, L - t0));
 
     // cluster mode: this chunk's o [G][D] fp32, in the K tiles' space once the
     // MMAs have completed; (m, l) per head are red[h], red[NH + h]
