@@ -115,26 +115,52 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = s * C;
     const size_t hq0 = (size_t)b * Hq + (size_t)g * G;
-    // The chunk's K and V boxes into L2 ahead of the dependency wait.  L2 is
-    // the point of coherence, so rows the previous kernel writes later are
-    // updated there; the length read here only decides whether to fetch.
+    // the chunk's K and V rows: KT boxes of 64 rows x 64 dims each; row
+    // (b Hkv + g) Lmax + t0 of the [B Hkv Lmax][D] view (rows past the end of
+    // the cache read as zero, rows past this sequence's length are masked)
+    const int row0 = (b * Hkv + g) * Lmax + t0;
+    auto issue_kv = [&]() {
+        mbar_arrive_expect_tx(kbar, KT * LY::TILE);
+        for (int c = 0; c < KT; ++c) tma_load_2d(sbase + LY::OFF_K + c * LY::TILE, &tm_k, c * 64, row0, smem_u32(kbar));
+        mbar_arrive_expect_tx(vbar, KT * LY::TILE);
+        for (int c = 0; c < KT; ++c) tma_load_2d(sbase + LY::OFF_V + c * LY::TILE, &tm_v, c * 64, row0, smem_u32(vbar));
+    };
+    // Ahead of the dependency wait only L2 is touched: the chunk's K and V
+    // boxes are prefetched there (L2 is the point of coherence, so rows the
+    // previous kernel writes later are updated there).  The length read here
+    // is a hint: it decides whether to prefetch, and whether thread 0 starts
+    // the copies into shared memory right after the wait, before the length
+    // the kernel uses (read after the wait) has arrived.
+    bool early = false;
     if (threadIdx.x == 0) {
         const int Lh = lens[b];
-        if (Lh > t0 && t0 < Lmax) {
-            const int row0 = (b * Hkv + g) * Lmax + t0;
+        early = Lh > t0 && t0 < Lmax;
+        if (early) {
             for (int c = 0; c < KT; ++c) {
                 tma_prefetch_2d(&tm_k, c * 64, row0);
                 tma_prefetch_2d(&tm_v, c * 64, row0);
             }
         }
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        fence_barrier_init();
     }
     // q, the lengths and the output buffers may come from the previous kernel
     // on the stream
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (early) issue_kv();
+    }
     int L = lens[b];
     L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
     const int n = max(0, min(C, L - t0));
+    if (n == 0 && early) {
+        // the hint was stale: the copies must land before their space is reused
+        // or the CTA leaves
+        mbar_wait_bounded(kbar, 0, budget, status);
+        mbar_wait_bounded(vbar, 0, budget, status);
+    }
+    if (n == 0) __syncthreads();
 
     // cluster mode: this chunk's o [G][D] fp32, in the K tiles' space once the
     // MMAs have completed; (m, l) per head are red[h], red[NH + h]
@@ -173,18 +199,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             if (i < QN && h < G) qv[j] = *reinterpret_cast<const uint4 *>(q + (hq0 + h) * D + d0);
         }
 
-        // the chunk's K and V rows: KT boxes of 64 rows x 64 dims each; row
-        // (b Hkv + g) Lmax + t0 of the [B Hkv Lmax][D] view (rows past the end of
-        // the cache read as zero, rows past this sequence's length are masked)
-        if (threadIdx.x == 0) {
-            for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
-            fence_barrier_init();
-            const int row0 = (b * Hkv + g) * Lmax + t0;
-            mbar_arrive_expect_tx(kbar, KT * LY::TILE);
-            for (int c = 0; c < KT; ++c) tma_load_2d(sbase + LY::OFF_K + c * LY::TILE, &tm_k, c * 64, row0, smem_u32(kbar));
-            mbar_arrive_expect_tx(vbar, KT * LY::TILE);
-            for (int c = 0; c < KT; ++c) tma_load_2d(sbase + LY::OFF_V + c * LY::TILE, &tm_v, c * 64, row0, smem_u32(vbar));
-        }
+        if (threadIdx.x == 0 && !early) issue_kv();      // the hint said empty
         if (warp == 0) tmem_alloc_cols(smem_u32((const void *)tslot), TCOLS);
     #pragma unroll
         for (int j = 0; j < QPT; ++j) {
