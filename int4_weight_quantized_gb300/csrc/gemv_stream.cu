@@ -9,10 +9,11 @@
 //     layout is row-major, the range is one contiguous byte range, copied in
 //     chunks of CR whole rows (weights and their fp16 block scales) by one
 //     producer warp with cp.async.bulk into an S-deep ring;
-//   - the first S chunks are requested before the kernel waits for the
-//     previous kernel on the stream (programmatic dependent launch), so a
-//     call's weight reads overlap the tail of the call before it; only the
-//     activations and the output depend on earlier work;
+//   - the first S chunks, and an L2 prefetch of the activations, are
+//     requested before the kernel waits for the previous kernel on the
+//     stream (programmatic dependent launch), so a call's weight reads
+//     overlap the tail of the call before it; only the activations and the
+//     output depend on earlier work;
 //   - activations are then quantised in the kernel (the pages' in-kernel
 //     activation quantisation) into shared memory, and every lane keeps the
 //     codes of its K blocks (l, l+32, l+64, ...) in registers;
@@ -20,7 +21,10 @@
 //     16-byte blocks of the row from the ring (32 int4 weights each), does
 //     8 dp4a per block and token and one fp32 multiply-add with s_w * s_x,
 //     and the 32 lanes are summed with shuffles; the warp then stores the
-//     row's outputs itself, so no cross-warp reduction is needed.
+//     row's outputs itself, so no cross-warp reduction is needed;
+//   - for one token with long rows the K blocks form 2 or 4 groups and as
+//     many warps share each row, one group each; their partial sums meet in
+//     shared memory and are added in group order.
 // Packed weights are stored as w + 8: dp4a of the unsigned nibbles gives
 // d + 8*sum(q), and starting the integer accumulator at 0x4B400000 - 8*sum(q)
 // leaves the float 1.5*2^23 + d, from which d follows exactly by one fp32
