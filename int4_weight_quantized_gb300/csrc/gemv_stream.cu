@@ -60,6 +60,7 @@ constexpr int STAGE_TARGET = 65536;         // weight bytes per chunk (at least;
                                             // shorten the work after the dependency wait)
 constexpr int SMEM_COTENANT = 110 * 1024;   // two CTAs per SM: the next launch's copies start early
 constexpr int SMEM_ALONE = 200 * 1024;      // one CTA per SM, for long rows or many tokens
+constexpr int SMEM_WHOLE = 224 * 1024;      // one CTA per SM whose rows all fit the ring at once
 constexpr int RG_MAX = 4;                   // rows reduced together per warp (compile-time bound)
 
 struct StreamArgs {
@@ -269,12 +270,15 @@ __global__ void __launch_bounds__(Warps<MT, BPL, GATED ? 2 : 1>::THREADS, Warps<
     {
         // When all of x takes two rounds of the consumer threads, both
         // rounds' loads are issued before either is quantised (one load
-        // latency instead of two); longer x keeps one load per round
-        // (batching more rounds measured slower there).
+        // latency instead of two); in the four-group instantiation (one
+        // token, K > 8192) x of more than four rounds goes four rounds at a
+        // time; otherwise longer x keeps one load per round (batched, three
+        // or four rounds measured slower, and a four-wide batch in the code
+        // slowed the other instantiations).
         const int items = MT * a.nb * 4;
-        constexpr int XB = Warps<MT, BPL, NV>::LIGHT ? 1 : 2;
+        constexpr int XB = Warps<MT, BPL, NV>::LIGHT ? 1 : (KG >= 4 ? 4 : 2);
         constexpr int STRIDE = CWARPS * 32;
-        const int xb = items <= XB * STRIDE ? XB : 1;
+        const int xb = XB == 1 ? 1 : (items <= 2 * STRIDE ? 2 : (XB == 4 && items > 4 * STRIDE ? 4 : 1));
         for (int base0 = 0; base0 < items; base0 += xb * STRIDE) {
             uint4 xv[XB];
             uint2 cv[XB];
@@ -559,7 +563,9 @@ void pick_codes(int MT, int nb, int &bpl, int &kg) {
 // slot is always being filled while another is read; the ring is sized, in
 // this order, for co-resident CTAs (the lightest register footprints: the
 // next launches' copies then start during this one) with three slots, for
-// one CTA per SM with three slots, and the same with two.  Within each
+// one CTA per SM holding all of its rows at once in up to three chunks (up
+// to 224 KB), for one CTA
+// per SM with three slots (200 KB), and the last two with two.  Within each
 // budget the largest chunk wins, but not one below a row per row slot while
 // another budget remains.
 Plan make_plan(int M, int N, int K, int nv = 1) {
@@ -597,14 +603,17 @@ Plan make_plan(int M, int N, int K, int nv = 1) {
         size_t limit;
         int min_slots;
     };
-    const Budget budgets[] = {{(size_t)SMEM_COTENANT, 3}, {(size_t)SMEM_ALONE, 3}, {(size_t)SMEM_COTENANT, 2},
-                              {(size_t)SMEM_ALONE, 2}};
+    // min_slots STAGES + 1: every chunk of the CTA in flight at once
+    const Budget budgets[] = {{(size_t)SMEM_COTENANT, 3}, {(size_t)SMEM_WHOLE, STAGES + 1}, {(size_t)SMEM_ALONE, 3},
+                              {(size_t)SMEM_COTENANT, 2}, {(size_t)SMEM_ALONE, 2}};
     bool ok = false;
     for (const Budget &b : budgets) {
         if (b.limit == (size_t)SMEM_COTENANT && !share) continue;
         for (int cr = cr0; cr >= 1 && !ok; --cr) {
             ok = fit(cr, b.limit, b.min_slots);
             if (ok && cr < row_slots && cr < cr0) ok = false;
+            // all in flight: at most three chunks (more, smaller ones measured slower)
+            if (ok && b.min_slots > STAGES && (p.nslots < (p.R + cr - 1) / cr || p.nslots > 3)) ok = false;
         }
         if (ok) break;
     }
@@ -622,7 +631,7 @@ template <int MT, int BPL, int KG, bool DEBUG, bool GATED, bool Q8>
 w4a8_status launch_t(const Plan &p, const StreamArgs &a, cudaStream_t stream) {
     auto kern = gemv_stream_kernel<MT, BPL, KG, DEBUG, GATED, Q8>;
     static std::atomic<int> attr_done[w4a8_host::kDeviceSlots];
-    const w4a8_status ast = w4a8_host::ensure_smem_limit(kern, SMEM_ALONE, attr_done);
+    const w4a8_status ast = w4a8_host::ensure_smem_limit(kern, SMEM_WHOLE, attr_done);
     if (ast != W4A8_OK) return ast;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
