@@ -119,6 +119,16 @@ int w4a8_mid_splits(int M, int N, int K);
  * Informational: w4a8_linear and w4a8_linear_ex choose it themselves. */
 int w4a8_prefill_splits(int M, int N, int K);
 
+/* Debug (host only, no device work): the launch plan of the streaming decode
+ * kernel for the first slice of up to 8 tokens of this shape (gated = 1: the
+ * gated kernel over 2N stacked rows).  plan, when not NULL, receives 10
+ * ints: tokens in the slice, activation-code slices per lane (0: codes in
+ * shared memory), K groups (warps sharing a row), weight rows per CTA, rows
+ * per ring chunk, ring slots, bytes per slot, dynamic shared memory per CTA,
+ * CTAs, rows per warp and pass.  Returns 1 when the kernel takes the shape,
+ * 0 otherwise (including an invalid shape). */
+int w4a8_debug_decode_plan(int M, int N, int K, int gated, int *plan);
+
 /* Device workspace in bytes that w4a8_linear_ex needs for this shape and
  * path (W4A8_PATH_AUTO resolves as w4a8_select_path); 0 when none.  The
  * prefill and mid paths keep the quantised activations there. */

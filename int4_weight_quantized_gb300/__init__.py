@@ -77,6 +77,8 @@ def lib():
         L.w4a8_get_device_status.argtypes = [P]
         L.w4a8_set_wait_budget.argtypes = [ctypes.c_longlong]
         L.w4a8_debug_wait_timeout.argtypes = [P]
+        L.w4a8_debug_decode_plan.argtypes = [i, i, i, i, P]
+        L.w4a8_debug_decode_plan.restype = i
         for f in ("w4a8_pack", "w4a8_linear", "w4a8_linear_ex", "w4a8_linear_gated", "w4a8_rmsnorm_quant",
                   "w4a8_linear_q8", "w4a8_decode_attention", "w4a8_linear_prefill_noalloc", "w4a8_debug_quantize_act",
                   "w4a8_debug_block_dots", "w4a8_debug_stream_read", "w4a8_get_device_status", "w4a8_set_wait_budget",
@@ -121,6 +123,19 @@ def select_path(M, N, K):
 def prefill_splits(M, N, K):
     """CTAs along K per output tile that the prefill path uses (1, 2, 4 or 8)."""
     return lib().w4a8_prefill_splits(M, N, K)
+
+
+DECODE_PLAN_FIELDS = ("tokens", "code_slices", "k_groups", "rows_per_cta", "rows_per_chunk", "ring_slots",
+                      "slot_bytes", "smem_bytes", "ctas", "rows_per_pass")
+
+
+def debug_decode_plan(M, N, K, gated=False):
+    """The streaming decode kernel's launch plan (host only): a dict of
+    DECODE_PLAN_FIELDS, or None when the kernel does not take the shape."""
+    buf = (ctypes.c_int * len(DECODE_PLAN_FIELDS))()
+    if not lib().w4a8_debug_decode_plan(M, N, K, 1 if gated else 0, ctypes.cast(buf, ctypes.c_void_p)):
+        return None
+    return dict(zip(DECODE_PLAN_FIELDS, list(buf)))
 
 
 def mid_splits(M, N, K):

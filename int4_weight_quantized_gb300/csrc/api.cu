@@ -134,6 +134,11 @@ int w4a8_select_path(int M, int N, int K) {
     return W4A8_PATH_PREFILL;
 }
 
+int w4a8_debug_decode_plan(int M, int N, int K, int gated, int *plan) {
+    if (!shape_ok(M, N, K) || (gated != 0 && gated != 1)) return 0;
+    return gemv_stream_plan_info(M, N, K, gated ? 2 : 1, plan) ? 1 : 0;
+}
+
 int w4a8_mid_splits(int M, int N, int K) {
     if (!shape_ok(M, N, K) || !mid_supported(M, N, K)) return 0;
     return tc_splits(M, N, K);

@@ -689,6 +689,15 @@ namespace w4a8_host {
 
 bool gemv_stream_supported(int M, int N, int K) { return make_plan(M < 8 ? M : 8, N, K).ok; }
 
+bool gemv_stream_plan_info(int M, int N, int K, int nv, int *out) {
+    const Plan p = make_plan(M < 8 ? M : 8, N, K, nv);
+    if (out) {
+        const int v[kPlanFields] = {p.MT, p.BPL, p.KG, p.R, p.cr, p.nslots, (int)p.stage_bytes, (int)p.smem, p.grid, p.rg};
+        for (int i = 0; i < kPlanFields; ++i) out[i] = v[i];
+    }
+    return p.ok;
+}
+
 bool gemv_stream_preferred(int M, int N, int K) {
     const Plan p = make_plan(M < 8 ? M : 8, N, K);
     return p.ok && (p.BPL > 0 || p.MT <= 2);

@@ -34,6 +34,12 @@ bool gemv_stream_supported(int M, int N, int K);
 // its activation codes in registers or there are at most two tokens;
 // otherwise the cluster split-K kernel (when it supports the shape) is faster.
 bool gemv_stream_preferred(int M, int N, int K);
+// The streaming decode kernel's launch plan for the first (up to 8-token)
+// slice of M (nv = 2 for the gated kernel), as kPlanFields ints: tokens,
+// code slices per lane, K groups, rows per CTA, rows per chunk, ring slots,
+// bytes per slot, dynamic shared memory, CTAs, rows per warp and pass.
+constexpr int kPlanFields = 10;
+bool gemv_stream_plan_info(int M, int N, int K, int nv, int *out);
 // Gated pair (gate rows 0..N-1 over up rows N..2N-1 of one packed matrix):
 // out[m][n] = act(gate_n . x_m) * (up_n . x_m), act 1 = SiLU, 2 = GELU (tanh).
 // Decode GEMV on activations quantised by their producer: codes int8 [M][K]

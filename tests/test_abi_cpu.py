@@ -166,3 +166,71 @@ def test_new_workspace_sizes(L):
     assert L.w4a8_prefill_splits(16, 128, 1056) == 8      # K % 256 != 0: the 128 x 128-tile kernel
     assert L.w4a8_prefill_splits(100, 256, 4096) == 8     # 128-token tiles of the streaming kernel
     assert L.w4a8_prefill_splits(0, 128, 1024) == 0
+
+
+def _plan(M, N, K, gated=False):
+    import int4_weight_quantized_gb300 as w4
+    return w4.debug_decode_plan(M, N, K, gated)
+
+
+def test_decode_plan_invariants(L):
+    """The streaming decode kernel's launch plan (host arithmetic only) stays
+    inside the hardware's limits and covers every row and K block, over a
+    grid of shapes and both the plain and the gated kernel."""
+    Ms = (1, 2, 3, 4, 5, 8, 9, 16)
+    Ns = (1, 7, 64, 256, 300, 2048, 4096, 8192, 14336, 28672)
+    Ks = (32, 96, 256, 1024, 2048, 3072, 4096, 6176, 8192, 10240, 14336, 16384, 28672)
+    checked = 0
+    for gated in (False, True):
+        nv = 2 if gated else 1
+        for M in Ms:
+            for N in Ns:
+                for K in Ks:
+                    p = _plan(M, N, K, gated)
+                    if p is None:
+                        continue
+                    checked += 1
+                    nb = K // 32
+                    MT = min(M, 8)
+                    assert p["tokens"] == MT
+                    assert 1 <= p["ring_slots"] <= 8
+                    assert 1 <= p["rows_per_chunk"] <= p["rows_per_cta"]
+                    assert p["slot_bytes"] % 16 == 0
+                    assert p["slot_bytes"] >= p["rows_per_chunk"] * nv * K // 2
+                    assert p["smem_bytes"] <= 224 * 1024
+                    assert p["smem_bytes"] >= p["ring_slots"] * p["slot_bytes"] + MT * nb * 32
+                    assert 1 <= p["ctas"] <= 152
+                    assert p["ctas"] * p["rows_per_cta"] >= N > (p["ctas"] - 1) * p["rows_per_cta"]
+                    chunks = -(-p["rows_per_cta"] // p["rows_per_chunk"])
+                    assert p["ring_slots"] <= chunks
+                    if p["ring_slots"] < chunks:
+                        assert p["ring_slots"] >= 2            # a refilled ring never has one slot
+                    assert p["code_slices"] in (0, 1, 2, 4, 8)
+                    assert p["k_groups"] in (1, 2, 4)
+                    if p["code_slices"]:
+                        assert p["code_slices"] * 32 * p["k_groups"] >= nb
+                        assert MT * p["code_slices"] <= 8
+                    if p["k_groups"] > 1:
+                        assert MT == 1 and p["code_slices"] == 4
+                        assert 8 % p["k_groups"] == 0
+                    assert p["rows_per_pass"] == min(8 // MT, 4)
+    assert checked > 1000
+
+
+def test_decode_plans_of_the_workloads(L):
+    # headline FFN up: one 54-row chunk, small enough for three CTAs per SM
+    p = _plan(1, 8192, 2048)
+    assert (p["code_slices"], p["k_groups"], p["rows_per_chunk"], p["ring_slots"]) == (2, 1, 54, 1)
+    assert 3 * (p["smem_bytes"] + 1024) <= 228 * 1024
+    # 14336 x 4096: all 95 rows of a CTA in flight in three chunks
+    p = _plan(1, 14336, 4096)
+    assert p["ring_slots"] == 3 and p["ring_slots"] * p["rows_per_chunk"] >= p["rows_per_cta"]
+    # long rows for one token: 4 slices of codes in 2 or 4 K groups
+    p = _plan(1, 2048, 8192)
+    assert (p["code_slices"], p["k_groups"], p["ring_slots"]) == (4, 2, 1)
+    p = _plan(1, 4096, 14336)
+    assert (p["code_slices"], p["k_groups"], p["ring_slots"]) == (4, 4, 3)
+    # several tokens keep one group: codes in registers while tokens x slices <= 8
+    assert _plan(2, 8192, 2048)["k_groups"] == 1
+    assert _plan(8, 129, 2048)["code_slices"] == 0
+    assert _plan(0, 8192, 2048) is None and _plan(1, 8192, 48) is None
