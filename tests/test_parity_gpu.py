@@ -175,7 +175,8 @@ def test_mid_path_split_counts(w4):
 # shared memory with one or two tokens); the others take the linear over 2N
 # rows and the element-wise pass
 GATED_SHAPES = [(1, 64, 64, True), (1, 300, 2048, True), (2, 96, 3072, True), (3, 130, 1024, True),
-                (8, 200, 256, True), (1, 1000, 4096, True), (1, 96, 8192, True), (5, 70, 4096, False),
+                (8, 200, 256, True), (1, 1000, 4096, True), (1, 96, 8192, True), (1, 64, 14336, True),
+                (5, 70, 4096, False),
                 (9, 70, 512, False),
                 (64, 128, 256, False), (200, 96, 320, False)]
 
