@@ -41,6 +41,12 @@ __global__ void __launch_bounds__(NT) rmsnorm_quant_kernel(const uint16_t *__res
                                                            uint16_t *__restrict__ res_out, uint16_t *__restrict__ y_out,
                                                            int8_t *__restrict__ codes, float *__restrict__ sx) {
     __shared__ float part[NT / 32];
+    // Programmatic dependent launch: the next kernel on the stream (the
+    // linear on these codes) may start now and issue its weight copies; all
+    // this kernel reads may come from the kernel before it, so it waits for
+    // that one first.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int m = blockIdx.x;
     const int groups = K / 8;
     const size_t row = (size_t)m * K;
@@ -130,7 +136,19 @@ namespace w4a8_host {
 
 w4a8_status launch_rmsnorm_quant(const uint16_t *x, const uint16_t *res, const uint16_t *gamma, float eps, int M, int K,
                                  uint16_t *res_out, uint16_t *y_out, int8_t *codes, float *sx, cudaStream_t stream) {
-    rmsnorm_quant_kernel<<<M, NT, 0, stream>>>(x, res, gamma, eps, K, res_out, y_out, codes, sx);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)M, 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, rmsnorm_quant_kernel, x, res, gamma, eps, K, res_out, y_out, codes, sx) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A8_ERR_CUDA;
+    }
     return launch_status();
 }
 
